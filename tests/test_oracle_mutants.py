@@ -1,0 +1,89 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check that
+the pins in ``test_oracle_pins.py`` catch every one of them."""
+import os
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "rope_oracle.c")
+
+# (name, text in rope_oracle.c, replacement)
+MUTANTS = [
+    ("interleave sign of the rotated odd member",
+     "xrot[2 * p] = -xs[2 * p + 1];", "xrot[2 * p] = xs[2 * p + 1];"),
+    ("interleave sin element index",
+     "double sn = load_elem(sin, cs_dt, crow + j);", "double sn = load_elem(sin, cs_dt, crow + (j ^ 1));"),
+    ("interleave dropped sin term",
+     "double y = xs[j] * c + xrot[j] * sn;", "double y = xs[j] * c;"),
+    ("interleave cos taken from the pair's even slot",
+     "double c = load_elem(cos, cs_dt, crow + j);", "double c = load_elem(cos, cs_dt, crow + (j & ~(int64_t)1));"),
+    ("broadcast over N always",
+     "const int64_t cn = cs_shape[2] == 1 ? 0 : n;", "const int64_t cn = 0;"),
+    ("NeoX halves swapped",
+     "x1 = xr[i];\n      x2 = xr[half + i];", "x1 = xr[half + i];\n      x2 = xr[i];"),
+    ("o2 sign",
+     "double o2 = x2 * cosv[i] + x1 * sinv[i];", "double o2 = x2 * cosv[i] - x1 * sinv[i];"),
+    ("o1 transposed operands",
+     "double o1 = x1 * cosv[i] - x2 * sinv[i];", "double o1 = x1 * sinv[i] - x2 * cosv[i];"),
+    ("GPT-J output concatenated instead of interleaved",
+     "out[2 * i] = o1;\n      out[2 * i + 1] = o2;", "out[i] = o1;\n      out[half + i] = o2;"),
+    ("cos and sin halves swapped",
+     "cosv[i] = cos_sin[i];\n        sinv[i] = cos_sin[half + i];",
+     "cosv[i] = cos_sin[half + i];\n        sinv[i] = cos_sin[i];"),
+    ("mrope ignores the section row for cos",
+     "cosv[i] = cos_sin[k * R + i];", "cosv[i] = cos_sin[i];"),
+    ("mrope sin read from the cos half",
+     "sinv[i] = cos_sin[k * R + half + i];", "sinv[i] = cos_sin[k * R + i];"),
+    ("rounding ties away from zero",
+     "double m = nearbyint(ldexp(a, (f.p - 1) - E));", "double m = round(ldexp(a, (f.p - 1) - E));"),
+    ("rounding by truncation",
+     "double m = nearbyint(ldexp(a, (f.p - 1) - E));", "double m = trunc(ldexp(a, (f.p - 1) - E));"),
+    ("subnormal scale off by one",
+     "v = ldexp((double)frac, emin - (f.p - 1));", "v = ldexp((double)frac, emin - f.p);"),
+    ("exponent bias off by one",
+     "(int)efield - f.emax - (f.p - 1));", "(int)efield - f.emax - f.p);"),
+]
+
+PIN_TESTS = [name for name in dir(pins) if name.startswith("test_")]
+
+
+def _run_pins():
+    failures = []
+    for name in PIN_TESTS:
+        fn = getattr(pins, name)
+        params = getattr(fn, "pytestmark", [])
+        arg_sets = [{}]
+        for mark in params:
+            if mark.name != "parametrize":
+                continue
+            argnames = [a.strip() for a in mark.args[0].split(",")]
+            new = []
+            for base in arg_sets:
+                for v in mark.args[1]:
+                    vals = v if len(argnames) > 1 else (v,)
+                    new.append({**base, **dict(zip(argnames, vals))})
+            arg_sets = new
+        for kw in arg_sets:
+            try:
+                fn(**kw)
+            except Exception:  # noqa: BLE001 - any failure counts as caught
+                failures.append(name)
+                break
+        if failures:
+            return failures
+    return failures
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    text = open(SRC).read()
+    assert text.count(old) == 1, "mutation site not found: " + name
+    lib = oracle.build_copy(text.replace(old, new), str(tmp_path / "mutant.so"))
+    try:
+        oracle.use_library(lib)
+        caught = _run_pins()
+    finally:
+        oracle.use_library(None)
+    assert caught, "no pin caught: " + name
