@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark of the RoPE hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic inputs:
+  1. in-place partial interleave RoPE, x bf16 [4,4096,32,128], slice [64,128),
+     cos/sin fp32 [1,4096,1,64];
+  2. cache RoPE, NeoX, bf16, 16384 tokens, 32 query + 8 key heads of 128;
+  3. cache RoPE, GPT-J, fp16, 8192 tokens (8 x 1024), 16 + 16 heads of 256, R = 64;
+  4. cache mrope [16,24,24], NeoX, bf16, 32768 tokens, 28 + 4 heads of 128.
+Metric: achieved HBM GB/s of algorithmic bytes (read + write of rotated
+elements, cos/sin or one gathered cache row per token, positions), plus
+tokens/s, against the measured peak bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores on bounded samples of the same workloads.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "RoPE achieved HBM GB/s and tokens/s on 1 GB300 vs peak-bandwidth roofline"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+WORKLOAD_NAME = ("rope hot path: inplace bf16x/f32cs [4,4096,32,128] slice[64,128) + cache NeoX bf16 16384tok "
+                 "32q8k h128 + cache GPT-J f16 8192tok 16q16k h256 r64 + mrope[16,24,24] NeoX bf16 32768tok "
+                 "28q4k h128")
+
+
+# ----------------------------------------------------------------------------
+# workloads and byte model
+# ----------------------------------------------------------------------------
+
+def build_workloads():
+    import workloads as W
+    return [W.inplace_bf16_mixed(), W.cache_neox_bf16(), W.cache_gptj_f16_partial(), W.mrope_neox_bf16()]
+
+
+def algorithmic_bytes(case) -> int:
+    """Read + write of rotated elements, cos/sin (or one gathered cache row per
+    token), positions.  Pass-through columns are never touched and not counted."""
+    if hasattr(case, "x"):
+        B, S, N, D = case.x.shape
+        L = D if (case.start, case.end) == (0, 0) else case.end - case.start
+        xb = B * S * N * L * case.x.element_size() * 2
+        return xb + 2 * case.cos.numel() * case.cos.element_size()
+    T = case.tokens
+    heads = (case.query.shape[1] + case.key.shape[1]) // case.head_size
+    e = case.query.element_size()
+    return (T * heads * case.rotary_dim * e * 2 + T * case.rotary_dim * e
+            + case.positions.numel() * case.positions.element_size())
+
+
+def kernel_label(case) -> str:
+    return case.name
+
+
+# ----------------------------------------------------------------------------
+# distributed helpers
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []  # (monotonic time, sm, sm_max, power, hw, hw_thermal, sw_thermal, sw_power)
+        self.proc = None
+        self.thread = None
+        ident = None
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            u = getattr(props, "uuid", None)
+            if u is not None:
+                s = str(u)
+                ident = s if s.startswith("GPU-") else "GPU-" + s
+        except Exception:  # noqa: BLE001
+            ident = None
+        self.ident = ident
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.ident:
+            cmd += ["-i", self.ident]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm, smax = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            flags = [p.lower() == "active" for p in parts[4:8]]
+            self.samples.append((time.monotonic(), sm, smax, parts[2], *flags))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed_region"
+        if not inside:
+            inside = self.samples
+            window = "whole_run"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for s in inside:
+            for n, f in zip(names, s[4:8]):
+                if f:
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------
+# roofline helpers
+# ----------------------------------------------------------------------------
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "transformer_rope_positional_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(label: str):
+    """DRAM bytes per launch from the committed ncu summary of ``label``, or
+    None when there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = re.search(r"^kernel_source_sha256_16:\s*(\S+)", text, re.M)
+    if not src or src.group(1) != kernel_source_hash():
+        return None
+    m = re.search(r"^%s:\s*([0-9]+)" % re.escape(label), text, re.M)
+    return int(m.group(1)) if m else None
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from transformer_rope_positional_gb300 import build as B
+    B.build()
+    import transformer_rope_positional_gb300 as R
+
+    cases = build_workloads()
+    step_bytes = [algorithmic_bytes(c) for c in cases]
+    step_tokens = sum(c.tokens for c in cases)
+    total_bytes = sum(step_bytes)
+
+    # device-resident inputs and prepared launches
+    dev_tensors = []
+    calls = []
+    for c in cases:
+        if hasattr(c, "x"):
+            x, cs, sn = c.x.to(dev), c.cos.to(dev), c.sin.to(dev)
+            dev_tensors.append((x, cs, sn))
+            calls.append(R.prepare_inplace_partial(x, cs, sn, c.rotary_mode, [c.start, c.end]))
+        else:
+            p, q, k, cc = c.positions.to(dev), c.query.to(dev), c.key.to(dev), c.cache.to(dev)
+            dev_tensors.append((p, q, k, cc))
+            calls.append(R.prepare_with_sin_cos_cache(p, q, k, cc, c.head_size, c.rotary_dim, c.is_neox,
+                                                      c.mrope_section))
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        for call in calls:
+            call()
+    torch.cuda.synchronize()
+    if R.get_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    K = args.steps
+    nk = len(calls)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(K)]
+    launches0 = R.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_host0 = time.monotonic()
+    # keep the GPU busy while the host queues the timed steps (outside the timed region)
+    torch.cuda._sleep(int(2e6))
+    for s in range(K):
+        ev = events[s]
+        for i, call in enumerate(calls):
+            ev[i].record()
+            call()
+        ev[nk].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    t_host1 = time.monotonic()
+    launches = R.launch_count() - launches0
+    total_ms = events[0][0].elapsed_time(events[K - 1][nk])
+    per_kernel_ms = [[events[s][i].elapsed_time(events[s][i + 1]) for s in range(K)] for i in range(nk)]
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+
+    ms_step_local = total_ms / K
+    ms_step = max_over_ranks(ms_step_local, world, dev)
+    value = world * total_bytes / (ms_step * 1e-3) / 1e9
+    tokens_per_s = world * step_tokens / (ms_step * 1e-3)
+
+    peak, peak_kind = measured_peak()
+    kernels = []
+    for c, b, ms in zip(cases, step_bytes, per_kernel_ms):
+        avg = sum(ms) / len(ms)
+        kernels.append({"workload": kernel_label(c), "bytes_per_launch": b, "avg_us": round(avg * 1e3, 3),
+                        "median_us": round(statistics.median(ms) * 1e3, 3),
+                        "gbs": round(b / (avg * 1e-3) / 1e9, 1), "frac_of_peak": round(b / (avg * 1e-3) / 1e9 / peak, 4),
+                        "tokens": c.tokens})
+    dom = max(range(nk), key=lambda i: sum(per_kernel_ms[i]))
+    dom_avg_s = sum(per_kernel_ms[dom]) / K * 1e-3
+    achieved = step_bytes[dom] / dom_avg_s / 1e9
+    roofline = {"bound": "hbm", "kernel": kernel_label(cases[dom]), "achieved": round(achieved, 1),
+                "peak": peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+                if peak_kind == "measured" else "fallback", "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel_label(cases[dom])),
+                "algorithmic_bytes": step_bytes[dom]}
+
+    e2e = run_e2e(args, cases, dev_tensors, calls, world, dev, total_bytes)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cases, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtypes": "bf16,f16 (x: bf16; cos/sin f32)",
+                "data": "synthetic (seeded SplitMix64 + Box-Muller N(0,1); cos/sin tables from base 1e4 / 1e6)",
+                "tokens_per_s": round(tokens_per_s, 1),
+                "config": {"workload": WORKLOAD_NAME, "bytes_per_step": total_bytes, "tokens_per_step": step_tokens,
+                           "l2": "inputs larger than L2: %.2f GB per step vs %d MB L2; each kernel's buffers are "
+                                 "evicted by the others between its launches" % (total_bytes / 1e9, L2_BYTES >> 20),
+                           "parallelism": "replicas of the per-GPU workload (weak scaling), no collective"},
+                "per_kernel": kernels, "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clocks, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, cases, dev_tensors, calls, world, dev, total_bytes):
+    """Host buffers in, host buffers out: per step the inputs are copied from
+    pinned host memory, the operators run through the public API, and the
+    results are copied back to pinned host memory."""
+    host_in = []
+    host_out = []
+    h2d = d2h = 0
+    for c, dt in zip(cases, dev_tensors):
+        if hasattr(c, "x"):
+            ins = [c.x.pin_memory(), c.cos.pin_memory(), c.sin.pin_memory()]
+            outs = [torch.empty_like(c.x).pin_memory()]
+            pairs_in = list(zip(ins, dt))
+            pairs_out = [(outs[0], dt[0])]
+        else:
+            ins = [c.positions.pin_memory(), c.query.pin_memory(), c.key.pin_memory(), c.cache.pin_memory()]
+            outs = [torch.empty_like(c.query).pin_memory(), torch.empty_like(c.key).pin_memory()]
+            pairs_in = list(zip(ins, dt))
+            pairs_out = [(outs[0], dt[1]), (outs[1], dt[2])]
+        host_in.append(pairs_in)
+        host_out.append(pairs_out)
+        h2d += sum(h.numel() * h.element_size() for h, _ in pairs_in)
+        d2h += sum(h.numel() * h.element_size() for h, _ in pairs_out)
+
+    def step():
+        for pin, call, pout in zip(host_in, calls, host_out):
+            for h, d in pin:
+                d.copy_(h, non_blocking=True)
+            call()
+            for h, d in pout:
+                h.copy_(d, non_blocking=True)
+
+    K = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(max(1, min(args.warmup, 3))):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    ms = max_over_ranks(ms, world, dev)
+    return {"value": round(world * total_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": K,
+            "path": "pinned host -> device copy, C-ABI call, device -> pinned host copy, per workload"}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(case, tokens: int):
+    """The first ``tokens`` tokens of a workload as a standalone case."""
+    import workloads as W
+    if hasattr(case, "x"):
+        B, S, N, D = case.x.shape
+        s = max(1, min(S, tokens))
+        x = case.x[:1, :s].contiguous()
+        cos = case.cos[:, :s].contiguous() if case.cos.shape[1] != 1 else case.cos
+        sin = case.sin[:, :s].contiguous() if case.sin.shape[1] != 1 else case.sin
+        return W.InplaceCase(case.name, x, cos[:1], sin[:1], case.start, case.end)
+    t = max(1, min(case.tokens, tokens))
+    return W.CacheCase(case.name, case.positions[..., :t].contiguous(), case.query[:t].contiguous(),
+                       case.key[:t].contiguous(), case.cache, case.head_size, case.rotary_dim, case.is_neox,
+                       case.mrope_section)
+
+
+def run_oracle(case):
+    import oracle
+    if hasattr(case, "x"):
+        oracle.inplace_partial_rotary_mul(case.x, case.cos, case.sin, case.start, case.end)
+    else:
+        oracle.rope_with_sin_cos_cache(case.positions, case.query, case.key, case.cache, case.head_size,
+                                       case.is_neox, case.mrope_section)
+
+
+def time_oracle(samples):
+    t0 = time.perf_counter()
+    for s in samples:
+        run_oracle(s)
+    return time.perf_counter() - t0
+
+
+def sized_samples(cases, budget_s: float):
+    """Per-workload token samples whose oracle time adds up to about budget_s,
+    keeping each workload's share of the step's bytes."""
+    probe = [oracle_sample(c, 64) for c in cases]
+    t = time_oracle(probe)
+    probe_bytes = sum(algorithmic_bytes(p) for p in probe)
+    rate = probe_bytes / max(t, 1e-6)
+    total = sum(algorithmic_bytes(c) for c in cases)
+    frac = min(1.0, budget_s * rate / total)
+    return [oracle_sample(c, max(1, int(c.tokens * frac))) for c in cases], frac
+
+
+def cpu_baseline(cases, budget_s: float):
+    import oracle
+    oracle.build()
+    samples, frac = sized_samples(cases, budget_s)
+    secs = time_oracle(samples)
+    b = sum(algorithmic_bytes(s) for s in samples)
+    tok = sum(s.tokens for s in samples)
+    return {"value": round(b / secs / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "tokens_per_s": round(tok / secs, 1), "seconds": round(secs, 2),
+            "sample": "first %.2f%% of the tokens of each of the four workloads (%d tokens, %d bytes), "
+                      "binary64 scalar C oracle, one thread" % (100 * frac, tok, b)}
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cases = build_workloads()
+    steps = args.steps + args.warmup
+    per_step = max(0.02, min(0.5, args.reference_seconds / max(1, steps)))
+    samples, frac = sized_samples(cases, per_step)
+    for _ in range(args.warmup):
+        time_oracle(samples)
+    times = [time_oracle(samples) for _ in range(args.steps)]
+    secs = sum(times) / len(times)
+    b = sum(algorithmic_bytes(s) for s in samples)
+    tok = sum(s.tokens for s in samples)
+    value = b / secs / 1e9
+    sample = ("first %.3f%% of the tokens of each of the four workloads per step (%d tokens, %d bytes), "
+              "binary64 scalar C oracle, one thread" % (100 * frac, tok, b))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "tokens_per_s": round(tok / secs, 1),
+            "config": {"workload": WORKLOAD_NAME, "sample": sample},
+            "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle work for cpu_baseline")
+    ap.add_argument("--reference-seconds", type=float, default=120.0, help="oracle work for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

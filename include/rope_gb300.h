@@ -1,0 +1,168 @@
+/*
+ * rope_gb300.h -- C ABI of the GB300 (sm_103a) rotary position embedding library.
+ *
+ * Two operators, each one asynchronous call on a caller-given CUDA stream:
+ *
+ *   rope_inplace_partial     in-place partial-slice interleave RoPE on a BSND tensor
+ *   rope_with_sin_cos_cache  cos/sin-cache-indexed RoPE of query and key (rope / mrope,
+ *                            GPT-NeoX or GPT-J style)
+ *
+ * Sources (web pages, cited by title and section):
+ *  [IPRM] "CANN ops-transformer 的 aclnnInplacePartialRotaryMul 算子：Inplace
+ *         部分旋转位置编码接口详解与实现剖析"
+ *  [RSCC] "CANN ops-transformer 旋转位置编码算子 RopeWithSinCosCache 深度解析：
+ *         cache 化 RoPE 的计算原理与 aclnn 两段式调用实战"
+ *
+ * Memory and ownership.  Every tensor is described by a rope_tensor_t that the
+ * caller owns; `data` is a DEVICE pointer to contiguous row-major storage,
+ * borrowed for the duration of the call and of the work it enqueues.  The
+ * library allocates nothing, needs no workspace, and never synchronises the
+ * stream (except rope_get_device_error, which says so).  The two-phase
+ * "GetWorkspaceSize, then execute" interface of the pages collapses to one call
+ * because the workspace is always zero bytes.
+ *
+ * Arithmetic.  Half-precision inputs are widened to binary32; each output is
+ * a two-term dot product evaluated with Kahan's FMA-based difference of
+ * products (relative error <= 2^-23, see Jeannerod, Louvet & Muller, Math. Comp.
+ * 82 (2013)) and rounded once, to nearest even, to the output type.  Results
+ * are deterministic and do not depend on the launch shape.
+ *
+ * Errors.  Every argument check happens on the host before anything is
+ * enqueued; a failed check returns a status and enqueues nothing.  Status
+ * values 161001 and 161002 are the ones [IPRM §返回值与错误码] lists
+ * (ACLNN_ERR_PARAM_NULLPTR, ACLNN_ERR_PARAM_INVALID).  A CUDA launch error is
+ * returned as ROPE_ERR_CUDA; errors that happen while the work runs surface at
+ * the caller's next synchronisation, as with any CUDA launch.
+ */
+#ifndef ROPE_GB300_H_
+#define ROPE_GB300_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ROPE_ABI_VERSION 1
+
+typedef enum {
+  ROPE_F32 = 0,  /* IEEE binary32 */
+  ROPE_F16 = 1,  /* IEEE binary16 */
+  ROPE_BF16 = 2, /* bfloat16 */
+  ROPE_I64 = 3   /* int64 (positions only) */
+} rope_dtype_t;
+
+/* A borrowed, contiguous, row-major device tensor of 1 to 4 dimensions. */
+typedef struct {
+  void* data;       /* device pointer; may be NULL only if the tensor is empty */
+  int32_t dtype;    /* a rope_dtype_t value */
+  int32_t ndim;     /* 1..4 */
+  int64_t shape[4]; /* shape[i] for i < ndim; entries past ndim are ignored */
+} rope_tensor_t;
+
+enum {
+  ROPE_OK = 0,
+  ROPE_ERR_PARAM_NULLPTR = 161001, /* a required tensor (or its data) is NULL */
+  ROPE_ERR_PARAM_INVALID = 161002, /* dtype, shape, slice, mode or alignment not supported */
+  ROPE_ERR_CUDA = 561000           /* the CUDA runtime refused a call (launch or query) */
+};
+
+/* Codes reported by rope_get_device_error. */
+enum {
+  ROPE_DEVICE_OK = 0,
+  ROPE_DEVICE_POSITION_OUT_OF_RANGE = 1 /* some position was < 0 or >= maxSeqLen */
+};
+
+/*
+ * In-place partial interleave RoPE.
+ * [IPRM §计算原理与公式, §partial_slice 局部旋转机制, §约束说明, §返回值与错误码]
+ *
+ * For every row r = (b, s, n) of x and every pair p of the slice (j = start + 2p):
+ *     x[r, j]   <- x[r, j]   * cos[r', 2p]   - x[r, j+1] * sin[r', 2p]
+ *     x[r, j+1] <- x[r, j+1] * cos[r', 2p+1] + x[r, j]   * sin[r', 2p+1]
+ * (the page's  x = x*cos + x_rotate*sin  with x_rotate built pair by pair from
+ * the negated odd member and the even member), where r' is r broadcast into
+ * cos/sin's [cB, cS, cN] dims.  Columns outside [start, end) are never read
+ * or written.
+ *
+ *   x            [B, S, N, D]; F32, F16 or BF16; D even, D <= 1024.  Rewritten in place.
+ *   cos, sin     [cB, cS, cN, L] with L = end - start; each of cB, cS, cN is 1 or
+ *                equal to x's B, S, N.  Same dtype as x, or F32 when x is F16/BF16
+ *                (computed in binary32, the page's mixed-precision combination).
+ *   rotary_mode  must be 1 (interleave); 0 (half) is declared by the page but not open.
+ *   start, end   the slice [start, end) of the D axis.  [0, 0] means the whole axis;
+ *                any other start == end is a no-op that enqueues nothing.
+ *                0 <= start <= end <= D, and end - start even.
+ *   stream       a cudaStream_t (NULL: the legacy default stream).
+ *
+ * Returns ROPE_OK, ROPE_ERR_PARAM_NULLPTR, ROPE_ERR_PARAM_INVALID or ROPE_ERR_CUDA.
+ * An empty x (some dim 0) is ROPE_OK and enqueues nothing.
+ */
+int rope_inplace_partial(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_tensor_t* sin,
+                         int64_t rotary_mode, int64_t start, int64_t end, void* stream);
+
+/*
+ * Cache-indexed RoPE of query and key, in place.
+ * [RSCC §设计动机 (the three steps), §mrope 模式, §rope 模式, §rotate_half（GPT-NeoX style）,
+ *  §rotate_interleaved（GPT-J style）, §约束说明, §入参校验逻辑]
+ *
+ * Per token t: gather cosSin = cache[positions[t]] (mrope: one row per positions
+ * row), split it into cos = cosSin[:R/2] and sin = cosSin[R/2:] (mrope: index i
+ * of cos and sin comes from the row of the section holding i), then rotate the
+ * first R = rotary_dim columns of every head of query and key:
+ *   NeoX (is_neox != 0), i < R/2:
+ *     o[i] = x[i]*cos[i] - x[i+R/2]*sin[i];   o[i+R/2] = x[i+R/2]*cos[i] + x[i]*sin[i]
+ *   GPT-J (is_neox == 0), i < R/2:
+ *     o[2i] = x[2i]*cos[i] - x[2i+1]*sin[i];  o[2i+1] = x[2i+1]*cos[i] + x[2i]*sin[i]
+ * Columns [R, head_size) of every head pass through: never read or written.
+ *
+ *   positions      I64; [numTokens] (rope) or [m, numTokens] (mrope, m = mrope_section_len).
+ *                  8-byte aligned.
+ *   query, key     2-D [numTokens, numQHeads*head_size] / [numTokens, numKHeads*head_size],
+ *                  non-empty, same dtype (F32, F16 or BF16), 16-byte aligned.  Rewritten in
+ *                  place (the page's queryOut/keyOut alias queryIn/keyIn).
+ *   cos_sin_cache  2-D [maxSeqLen, R], same dtype as query, 16-byte aligned.
+ *   head_size      a multiple of 32 (F16/BF16) or 16 (F32), dividing both row widths.
+ *   rotary_dim     R; must equal cos_sin_cache.shape[1]; R <= head_size and a multiple of
+ *                  32 (F16/BF16) or 16 (F32).
+ *   is_neox        nonzero: GPT-NeoX rotate_half; zero: GPT-J rotate_interleaved.
+ *   mrope_section  HOST pointer to mrope_section_len int64 values, or NULL for rope mode.
+ *                  mrope is on when the pointer is non-NULL and mrope_section[0] > 0;
+ *                  then mrope_section_len is 3 or 4, every value >= 0, and
+ *                  2 * sum == R.  A non-NULL section whose first value is 0 means rope.
+ *   stream         a cudaStream_t (NULL: the legacy default stream).
+ *
+ * Positions outside [0, maxSeqLen) cannot be checked on the host: a token with such a
+ * position is left untouched and ROPE_DEVICE_POSITION_OUT_OF_RANGE is recorded for
+ * rope_get_device_error.
+ *
+ * Returns ROPE_OK, ROPE_ERR_PARAM_NULLPTR, ROPE_ERR_PARAM_INVALID or ROPE_ERR_CUDA.
+ */
+int rope_with_sin_cos_cache(const rope_tensor_t* positions, const rope_tensor_t* query,
+                            const rope_tensor_t* key, const rope_tensor_t* cos_sin_cache,
+                            int64_t head_size, int64_t rotary_dim, int32_t is_neox,
+                            const int64_t* mrope_section, int64_t mrope_section_len, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device-side error word of the
+ * current device.  *code receives ROPE_DEVICE_OK or a bitwise OR of the
+ * ROPE_DEVICE_* codes recorded by kernels since the last read (by any stream of
+ * this device).  Returns ROPE_OK, ROPE_ERR_PARAM_NULLPTR (code is NULL) or
+ * ROPE_ERR_CUDA.
+ */
+int rope_get_device_error(void* stream, int32_t* code);
+
+/* A static, human-readable name for a status value (never NULL). */
+const char* rope_status_string(int status);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t rope_launch_count(void);
+
+/* ROPE_ABI_VERSION of the built library. */
+int rope_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROPE_GB300_H_ */

@@ -1,0 +1,72 @@
+"""Comparison rules shared by the parity tests.
+
+Tolerances (written here, applied everywhere):
+
+* float32 outputs: relative error at most ``FP32_REL_TOL`` = 2e-6 against the
+  oracle, measured as |got - ref| / max(|ref|, 2^-126).  The kernels evaluate
+  each output with Kahan's difference of products (error <= 2^-23 relative) and
+  the oracle rounds the binary64 result once, so the expected gap is below
+  2.4e-7; 2e-6 is the stated bar.
+* float16 / bfloat16 outputs: at most ``HALF_ULP_TOL`` = 1 unit in the last place
+  of the output type.  The binary32 result is within 2^-23 of the exact value,
+  so narrowing it differs from narrowing the exact value by at most one ulp.
+* columns the operator must not touch: bit-exact.
+* NaN matches NaN (any payload); +0 matches -0; infinities must match exactly.
+"""
+import numpy as np
+import torch
+
+FP32_REL_TOL = 2e-6
+HALF_ULP_TOL = 1
+
+
+def same_bits(a: torch.Tensor, b: torch.Tensor) -> bool:
+    view = {8: torch.int64, 4: torch.int32, 2: torch.int16}[a.element_size()]
+    return torch.equal(a.detach().cpu().contiguous().view(view), b.detach().cpu().contiguous().view(view))
+
+
+def ulp_distance(a: torch.Tensor, b: torch.Tensor) -> np.ndarray:
+    a = a.detach().cpu().contiguous()
+    b = b.detach().cpu().contiguous()
+    view = {4: torch.int32, 2: torch.int16}[a.element_size()]
+    nbits = 8 * a.element_size()
+    ia = a.view(view).numpy().astype(np.int64) & ((1 << nbits) - 1)
+    ib = b.view(view).numpy().astype(np.int64) & ((1 << nbits) - 1)
+    sign = 1 << (nbits - 1)
+    oa = np.where(ia & sign, -(ia & (sign - 1)), ia)
+    ob = np.where(ib & sign, -(ib & (sign - 1)), ib)
+    d = np.abs(oa - ob)
+    na = torch.isnan(a.float()).numpy()
+    nb = torch.isnan(b.float()).numpy()
+    d = np.where(na & nb, 0, d)
+    return np.where(na ^ nb, 1 << 40, d)
+
+
+def compare(got: torch.Tensor, ref: torch.Tensor) -> dict:
+    """Error summary of ``got`` against the oracle's ``ref`` (same dtype)."""
+    assert got.dtype == ref.dtype and got.shape == ref.shape, (got.dtype, ref.dtype, got.shape, ref.shape)
+    g = got.detach().cpu()
+    r = ref.detach().cpu()
+    out = {"n": int(r.numel())}
+    if r.dtype == torch.float32:
+        gd = g.double().numpy()
+        rd = r.double().numpy()
+        both_nan = np.isnan(gd) & np.isnan(rd)
+        inf_ok = np.isinf(rd) & (gd == rd)
+        with np.errstate(invalid="ignore"):
+            rel = np.abs(gd - rd) / np.maximum(np.abs(rd), 2.0 ** -126)
+        rel = np.where(both_nan | inf_ok, 0.0, rel)
+        rel = np.where(np.isnan(rel), np.inf, rel)
+        out["max_rel"] = float(rel.max()) if rel.size else 0.0
+        out["ok"] = out["max_rel"] <= FP32_REL_TOL
+    else:
+        d = ulp_distance(g, r)
+        out["max_ulp"] = int(d.max()) if d.size else 0
+        out["ok"] = out["max_ulp"] <= HALF_ULP_TOL
+    return out
+
+
+def assert_matches(got: torch.Tensor, ref: torch.Tensor, what: str = "") -> dict:
+    res = compare(got, ref)
+    assert res["ok"], "%s: %s" % (what, res)
+    return res

@@ -1,0 +1,212 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments before touching the GPU.
+
+Nothing here launches a kernel: every call either fails validation or is a
+no-op that returns before any CUDA call, so the file runs on a machine without
+a GPU.  Fake device pointers are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from transformer_rope_positional_gb300 import _capi as C
+from transformer_rope_positional_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rope_gb300.h")
+FAKE = 0x10000  # a non-NULL, 64 KiB-aligned address that is never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return C.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rope_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(C.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.rope_abi_version() == 1
+    for st in (C.ROPE_OK, C.ROPE_ERR_PARAM_NULLPTR, C.ROPE_ERR_PARAM_INVALID, C.ROPE_ERR_CUDA, 12345):
+        s = C.status_string(st)
+        assert isinstance(s, str) and s
+    assert "NULLPTR" in C.status_string(161001) and "INVALID" in C.status_string(161002)
+
+
+def _d(dtype, shape, ptr=FAKE):
+    return C.describe(ptr, dtype, shape)
+
+
+def _inplace(lib, x, c, s, mode=1, start=0, end=0):
+    return lib.rope_inplace_partial(ctypes.byref(x) if x else None, ctypes.byref(c) if c else None,
+                                    ctypes.byref(s) if s else None, mode, start, end, None)
+
+
+X = (2, 3, 4, 64)
+CS = (1, 3, 1, 64)
+
+
+@pytest.mark.parametrize("which", [0, 1, 2])
+def test_inplace_null_descriptors(lib, which):
+    args = [_d(C.F32, X), _d(C.F32, CS), _d(C.F32, CS)]
+    args[which] = None
+    assert _inplace(lib, *args) == C.ROPE_ERR_PARAM_NULLPTR
+
+
+def test_inplace_null_data_pointer(lib):
+    # shapes are valid, so the missing data is what is reported
+    assert _inplace(lib, _d(C.F32, X, 0), _d(C.F32, CS), _d(C.F32, CS)) == C.ROPE_ERR_PARAM_NULLPTR
+
+
+@pytest.mark.parametrize("xdt,cdt,sdt,ok", [
+    (C.F32, C.F16, C.F16, False),    # f32 x needs f32 cos/sin
+    (C.F16, C.BF16, C.BF16, False),  # half x with the other half type
+    (C.F16, C.F32, C.F16, False),    # cos and sin differ
+    (C.I64, C.I64, C.I64, False),
+    (C.BF16, C.F32, C.F32, True),    # mixed precision is allowed
+])
+def test_inplace_dtype_rules(lib, xdt, cdt, sdt, ok):
+    st = _inplace(lib, _d(xdt, X), _d(cdt, CS), _d(sdt, CS), start=8, end=8)
+    assert st == (C.ROPE_OK if ok else C.ROPE_ERR_PARAM_INVALID)
+
+
+@pytest.mark.parametrize("mode", [0, 2, 3, -1])
+def test_inplace_only_interleave_mode(lib, mode):
+    assert _inplace(lib, _d(C.F32, X), _d(C.F32, CS), _d(C.F32, CS), mode=mode) == C.ROPE_ERR_PARAM_INVALID
+
+
+@pytest.mark.parametrize("xs,cs,start,end", [
+    ((2, 3, 64), (1, 3, 1, 64), 0, 0),          # x not 4-D
+    ((2, 3, 4, 1026), (1, 3, 1, 1026), 0, 0),   # D > 1024
+    ((2, 3, 4, 63), (1, 3, 1, 63), 0, 0),       # D odd
+    (X, (1, 3, 1, 8), -2, 6),                   # start < 0
+    (X, (1, 3, 1, 8), 60, 68),                  # end > D
+    (X, (1, 3, 1, 8), 10, 4),                   # start > end
+    (X, (1, 3, 1, 7), 3, 10),                   # odd slice length
+    (X, (1, 3, 1, 16), 0, 8),                   # cos last dim != slice length
+    (X, (3, 3, 1, 64), 0, 0),                   # cos B neither 1 nor B
+    (X, (1, 2, 1, 64), 0, 0),                   # cos S neither 1 nor S
+    (X, (1, 3, 2, 64), 0, 0),                   # cos N neither 1 nor N
+])
+def test_inplace_shape_rules(lib, xs, cs, start, end):
+    st = _inplace(lib, _d(C.F32, xs), _d(C.F32, cs), _d(C.F32, cs), start=start, end=end)
+    assert st == C.ROPE_ERR_PARAM_INVALID
+
+
+def test_inplace_cos_sin_shapes_must_match(lib):
+    st = _inplace(lib, _d(C.F32, X), _d(C.F32, CS), _d(C.F32, (1, 3, 4, 64)))
+    assert st == C.ROPE_ERR_PARAM_INVALID
+
+
+def test_inplace_noop_enqueues_nothing(lib):
+    before = lib.rope_launch_count()
+    # start == end (not [0,0]) is a no-op, checked before the cos width
+    assert _inplace(lib, _d(C.F32, X), _d(C.F32, (1, 3, 1, 5)), _d(C.F32, (1, 3, 1, 5)), start=8,
+                    end=8) == C.ROPE_OK
+    # an empty x is a no-op too
+    assert _inplace(lib, _d(C.F32, (0, 3, 4, 64)), _d(C.F32, (1, 3, 1, 64)), _d(C.F32, (1, 3, 1, 64)),
+                    start=0, end=0) == C.ROPE_OK
+    assert lib.rope_launch_count() == before
+
+
+def _cache(lib, pos, q, k, c, head_size=64, R=None, neox=1, section=None):
+    R = (c.shape[1] if c is not None else 64) if R is None else R
+    sec = None
+    n = 0
+    if section is not None:
+        n = len(section)
+        sec = (ctypes.c_int64 * max(1, n))(*section)
+    return lib.rope_with_sin_cos_cache(*(ctypes.byref(t) if t is not None else None for t in (pos, q, k, c)),
+                                       head_size, R, neox, sec, n, None)
+
+
+T = 7
+
+
+def good(dt=C.BF16, R=64, hs=64):
+    return (_d(C.I64, (T,)), _d(dt, (T, 4 * hs)), _d(dt, (T, 2 * hs)), _d(dt, (100, R)))
+
+
+@pytest.mark.parametrize("which", [0, 1, 2, 3])
+def test_cache_null_descriptors(lib, which):
+    args = list(good())
+    args[which] = None
+    assert _cache(lib, *args) == C.ROPE_ERR_PARAM_NULLPTR
+
+
+def test_cache_null_data(lib):
+    p, q, k, c = good()
+    q = _d(C.BF16, (T, 256), 0)
+    assert _cache(lib, p, q, k, c) == C.ROPE_ERR_PARAM_NULLPTR
+
+
+def _bad(lib, **kw):
+    p, q, k, c = good()
+    args = dict(pos=p, q=q, k=k, c=c, head_size=64, R=None, neox=1, section=None)
+    args.update(kw)
+    return _cache(lib, args["pos"], args["q"], args["k"], args["c"], args["head_size"], args["R"],
+                  args["neox"], args["section"])
+
+
+@pytest.mark.parametrize("case", [
+    dict(pos=_d(C.F32, (T,))),                                  # positions not int64
+    dict(k=_d(C.F16, (T, 128))),                                # key dtype differs
+    dict(c=_d(C.F16, (100, 64))),                               # cache dtype differs
+    dict(q=_d(C.BF16, (T, 4, 64))),                             # query not 2-D
+    dict(q=_d(C.BF16, (0, 256)), k=_d(C.BF16, (0, 128)), pos=_d(C.I64, (0,))),  # no tokens
+    dict(k=_d(C.BF16, (T + 1, 128))),                           # token counts differ
+    dict(head_size=48),                                         # not a multiple of 32 for bf16
+    dict(head_size=96),                                         # does not divide the row widths
+    dict(R=32),                                                 # rotary_dim != cache width
+    dict(c=_d(C.BF16, (100, 48)), R=48),                        # R not a multiple of 32
+    dict(c=_d(C.BF16, (100, 128)), R=128),                      # R > head_size
+    dict(pos=_d(C.I64, (T + 1,))),                              # positions length
+    dict(section=[16, 16]),                                     # section count not 3 or 4
+    dict(section=[16, 8, 4], pos=_d(C.I64, (3, T))),            # 2 * sum != R
+    dict(section=[16, -8, 24], pos=_d(C.I64, (3, T))),          # negative element
+    dict(section=[8, 12, 12]),                                  # mrope with 1-D positions
+    dict(section=[8, 12, 12], pos=_d(C.I64, (4, T))),           # rows != section count
+])
+def test_cache_rejections(lib, case):
+    assert _bad(lib, **case) == C.ROPE_ERR_PARAM_INVALID
+
+
+def test_cache_fp32_sizes_follow_16_element_rule(lib):
+    p, _, _, _ = good()
+    q = _d(C.F32, (T, 4 * 48))
+    k = _d(C.F32, (T, 2 * 48))
+    c = _d(C.F32, (100, 40))
+    # 48 is a multiple of 16 (allowed for fp32) but 40 is not
+    assert _cache(lib, p, q, k, c, head_size=48) == C.ROPE_ERR_PARAM_INVALID
+
+
+def test_cache_misaligned_pointers_rejected(lib):
+    p, q, k, c = good()
+    q = _d(C.BF16, (T, 256), FAKE + 2)
+    assert _cache(lib, p, q, k, c) == C.ROPE_ERR_PARAM_INVALID
+
+
+def test_device_error_needs_an_out_pointer(lib):
+    assert lib.rope_get_device_error(None, None) == C.ROPE_ERR_PARAM_NULLPTR
+
+
+def test_python_binding_refuses_cpu_tensors():
+    B.build()
+    x = torch.zeros(1, 2, 2, 8)
+    c = torch.ones(1, 2, 1, 8)
+    with pytest.raises(ValueError):
+        C.rope_inplace_partial(x, c, c)

@@ -1,0 +1,77 @@
+"""The five named workloads at full size, through the same library calls the
+benchmark times.
+
+The oracle recomputes a sample of tokens one by one (tokens are independent
+under both operators); properties that hold at any size -- untouched columns
+bit-exact, no device error -- are checked on the whole output.
+"""
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_runs import gpu_cache, gpu_inplace, oracle_inplace
+from parity import assert_matches, same_bits
+import transformer_rope_positional_gb300 as R
+
+pytestmark = pytest.mark.gpu
+
+SAMPLE = 384
+
+
+def _sample(n, seed):
+    idx = W.uniform_int(W.stream_seed(seed, 9), SAMPLE, 0, n)
+    return torch.unique(torch.cat([idx, torch.tensor([0, n - 1])]))
+
+
+@pytest.mark.parametrize("variant", ["slice", "full", "noop"])
+def test_small_f32_workload_whole(rope_gpu, variant):
+    case = W.inplace_f32_small(variant)
+    got = gpu_inplace(case)
+    assert_matches(got, oracle_inplace(case), case.name)
+
+
+def test_mixed_bf16_workload_full_size(rope_gpu):
+    case = W.inplace_bf16_mixed()
+    got = gpu_inplace(case)
+    assert R.get_device_error() == 0
+    B, S, N, D = case.x.shape
+    # columns [0, 64) are outside the slice: bit-exact over the whole tensor
+    assert same_bits(got[..., :64], case.x[..., :64])
+    tok = _sample(B * S, 101)
+    for t in tok.tolist():
+        b, s = divmod(t, S)
+        sub = W.InplaceCase("tok", case.x[b:b + 1, s:s + 1].contiguous(), case.cos[:, s:s + 1].contiguous(),
+                            case.sin[:, s:s + 1].contiguous(), case.start, case.end)
+        ref = oracle.inplace_partial_rotary_mul(sub.x, sub.cos, sub.sin, sub.start, sub.end)
+        assert_matches(got[b:b + 1, s:s + 1], ref, "token %d" % t)
+
+
+def _check_cache_sampled(case, seed):
+    qg, kg = gpu_cache(case)
+    assert R.get_device_error() == 0
+    T = case.tokens
+    tok = _sample(T, seed)
+    pos = case.positions[..., tok].contiguous()
+    qo, ko, skipped = oracle.rope_with_sin_cos_cache(pos, case.query[tok], case.key[tok], case.cache,
+                                                     case.head_size, case.is_neox, case.mrope_section)
+    assert skipped == 0
+    assert_matches(qg[tok], qo, case.name + " query")
+    assert_matches(kg[tok], ko, case.name + " key")
+    return qg, kg
+
+
+def test_neox_bf16_workload_full_size(rope_gpu):
+    _check_cache_sampled(W.cache_neox_bf16(), 102)
+
+
+def test_gptj_f16_partial_workload_full_size(rope_gpu):
+    case = W.cache_gptj_f16_partial()
+    qg, kg = _check_cache_sampled(case, 103)
+    hs, r = case.head_size, case.rotary_dim
+    for got, x in ((qg, case.query), (kg, case.key)):
+        assert same_bits(got.view(case.tokens, -1, hs)[..., r:], x.view(case.tokens, -1, hs)[..., r:])
+
+
+def test_mrope_workload_full_size(rope_gpu):
+    _check_cache_sampled(W.mrope_neox_bf16(), 104)

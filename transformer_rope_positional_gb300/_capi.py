@@ -1,0 +1,208 @@
+"""ctypes binding of ``librope_gb300.so`` (see ``include/rope_gb300.h``).
+
+Argument marshalling only: every step of both operators runs in the CUDA
+library.  The library must have been built (``python -m
+transformer_rope_positional_gb300.build``); there is no fallback, and calling
+an operator without it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "librope_gb300.so")
+
+F32, F16, BF16, I64 = 0, 1, 2, 3
+DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16, torch.int64: I64}
+
+ROPE_OK = 0
+ROPE_ERR_PARAM_NULLPTR = 161001
+ROPE_ERR_PARAM_INVALID = 161002
+ROPE_ERR_CUDA = 561000
+ROPE_DEVICE_POSITION_OUT_OF_RANGE = 1
+
+EXPORTED = ("rope_inplace_partial", "rope_with_sin_cos_cache", "rope_get_device_error",
+            "rope_status_string", "rope_launch_count", "rope_abi_version")
+
+
+class RopeTensor(ctypes.Structure):
+    """Mirror of ``rope_tensor_t``."""
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4)]
+
+
+class RopeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s failed with status %d (%s)" % (what, status, status_string(status)))
+        self.status = status
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("librope_gb300.so is not built (%s missing); run "
+                           "`python -m transformer_rope_positional_gb300.build`" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(RopeTensor)
+    lib.rope_inplace_partial.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_void_p]
+    lib.rope_inplace_partial.restype = ctypes.c_int
+    lib.rope_with_sin_cos_cache.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                            ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_void_p]
+    lib.rope_with_sin_cos_cache.restype = ctypes.c_int
+    lib.rope_get_device_error.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+    lib.rope_get_device_error.restype = ctypes.c_int
+    lib.rope_status_string.argtypes = [ctypes.c_int]
+    lib.rope_status_string.restype = ctypes.c_char_p
+    lib.rope_launch_count.argtypes = []
+    lib.rope_launch_count.restype = ctypes.c_uint64
+    lib.rope_abi_version.argtypes = []
+    lib.rope_abi_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().rope_status_string(int(status)).decode()
+
+
+def describe(data_ptr: int, dtype_code: int, shape: Sequence[int]) -> RopeTensor:
+    """A ``rope_tensor_t`` from a raw device pointer (no checks here)."""
+    d = RopeTensor()
+    d.data = data_ptr or None
+    d.dtype = dtype_code
+    d.ndim = len(shape)
+    for i, s in enumerate(shape):
+        d.shape[i] = int(s)
+    return d
+
+
+def tensor_desc(t: torch.Tensor) -> RopeTensor:
+    """Describe a contiguous CUDA tensor."""
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor, got one on %s" % t.device)
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if t.dtype not in DTYPE_CODE:
+        raise ValueError("unsupported dtype %s" % t.dtype)
+    return describe(t.data_ptr(), DTYPE_CODE[t.dtype], tuple(t.shape))
+
+
+def _stream_handle(t: torch.Tensor, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def rope_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode: int = 1,
+                         partial_slice: Optional[Sequence[int]] = None, stream=None) -> None:
+    """In-place partial interleave RoPE of ``x`` [B, S, N, D] over ``partial_slice``.
+
+    ``partial_slice=None`` means ``[0, 0]``, the whole D axis.  Returns None; x
+    is rewritten on ``stream`` (default: the current stream of x's device).
+    """
+    start, end = (0, 0) if partial_slice is None else (int(partial_slice[0]), int(partial_slice[1]))
+    if partial_slice is not None and len(partial_slice) != 2:
+        raise RopeError(ROPE_ERR_PARAM_INVALID, "rope_inplace_partial")
+    lib = load()
+    dx, dc, ds = tensor_desc(x), tensor_desc(cos), tensor_desc(sin)
+    st = lib.rope_inplace_partial(ctypes.byref(dx), ctypes.byref(dc), ctypes.byref(ds), int(rotary_mode),
+                                  start, end, _stream_handle(x, stream))
+    if st != ROPE_OK:
+        raise RopeError(st, "rope_inplace_partial")
+
+
+def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: torch.Tensor,
+                            cos_sin_cache: torch.Tensor, head_size: int, rotary_dim: Optional[int] = None,
+                            is_neox: bool = True, mrope_section: Optional[Sequence[int]] = None,
+                            stream=None) -> None:
+    """Cache-indexed RoPE of ``query`` and ``key`` in place (rope or mrope mode)."""
+    lib = load()
+    R = int(cos_sin_cache.shape[1]) if rotary_dim is None else int(rotary_dim)
+    dp, dq, dk, dc = (tensor_desc(positions), tensor_desc(query), tensor_desc(key),
+                      tensor_desc(cos_sin_cache))
+    sec = None
+    n_sec = 0
+    if mrope_section is not None:
+        n_sec = len(mrope_section)
+        sec = (ctypes.c_int64 * max(1, n_sec))(*[int(v) for v in mrope_section])
+    st = lib.rope_with_sin_cos_cache(ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc),
+                                     int(head_size), R, 1 if is_neox else 0, sec, n_sec,
+                                     _stream_handle(query, stream))
+    if st != ROPE_OK:
+        raise RopeError(st, "rope_with_sin_cos_cache")
+
+
+def get_device_error(stream=None, device=None) -> int:
+    """Synchronise ``stream`` and read-and-clear the device error word."""
+    lib = load()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    code = ctypes.c_int32(0)
+    st = lib.rope_get_device_error(handle, ctypes.byref(code))
+    if st != ROPE_OK:
+        raise RopeError(st, "rope_get_device_error")
+    return int(code.value)
+
+
+def launch_count() -> int:
+    return int(load().rope_launch_count())
+
+
+class PreparedCall:
+    """One operator call with its C arguments marshalled once.
+
+    Calling it re-issues the same launch on the same tensors (for loops that
+    apply the operator many times); it keeps the tensors alive.
+    """
+
+    def __init__(self, fn, args, keep, what):
+        self._fn = fn
+        self._args = args
+        self._keep = keep
+        self._what = what
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != ROPE_OK:
+            raise RopeError(st, self._what)
+
+
+def prepare_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode: int = 1,
+                            partial_slice: Optional[Sequence[int]] = None, stream=None) -> PreparedCall:
+    lib = load()
+    start, end = (0, 0) if partial_slice is None else (int(partial_slice[0]), int(partial_slice[1]))
+    dx, dc, ds = tensor_desc(x), tensor_desc(cos), tensor_desc(sin)
+    args = (ctypes.byref(dx), ctypes.byref(dc), ctypes.byref(ds), int(rotary_mode), start, end,
+            _stream_handle(x, stream))
+    return PreparedCall(lib.rope_inplace_partial, args, (x, cos, sin, dx, dc, ds), "rope_inplace_partial")
+
+
+def prepare_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: torch.Tensor,
+                               cos_sin_cache: torch.Tensor, head_size: int, rotary_dim: Optional[int] = None,
+                               is_neox: bool = True, mrope_section: Optional[Sequence[int]] = None,
+                               stream=None) -> PreparedCall:
+    lib = load()
+    R = int(cos_sin_cache.shape[1]) if rotary_dim is None else int(rotary_dim)
+    dp, dq, dk, dc = (tensor_desc(positions), tensor_desc(query), tensor_desc(key),
+                      tensor_desc(cos_sin_cache))
+    sec = None
+    n_sec = 0
+    if mrope_section is not None:
+        n_sec = len(mrope_section)
+        sec = (ctypes.c_int64 * max(1, n_sec))(*[int(v) for v in mrope_section])
+    args = (ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc), int(head_size), R,
+            1 if is_neox else 0, sec, n_sec, _stream_handle(query, stream))
+    return PreparedCall(lib.rope_with_sin_cos_cache, args,
+                        (positions, query, key, cos_sin_cache, dp, dq, dk, dc, sec), "rope_with_sin_cos_cache")

@@ -1,0 +1,207 @@
+// C ABI of the RoPE library: argument checks, dispatch, status strings.
+//
+// The checks follow the constraint and error-code lists of the two operator
+// pages ("CANN ops-transformer 的 aclnnInplacePartialRotaryMul 算子…", sections
+// 返回值与错误码 and 约束说明; "CANN ops-transformer 旋转位置编码算子
+// RopeWithSinCosCache 深度解析…", sections 约束说明 and 入参校验逻辑).  Every check
+// runs on the host before anything is enqueued, and no check touches the GPU,
+// so a rejected call has no side effect at all.
+#include <atomic>
+#include <mutex>
+
+#include "../../include/rope_gb300.h"
+#include "rope_launch.h"
+
+namespace rope {
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+constexpr int kMaxDevices = 64;
+std::once_flag g_sm_once[kMaxDevices];
+int g_sm_count[kMaxDevices];
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::call_once(g_sm_once[dev], [dev] {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_sm_count[dev] = n;
+  });
+  return g_sm_count[dev];
+}
+
+}  // namespace rope
+
+namespace {
+
+using rope::kBF16;
+using rope::kF16;
+using rope::kF32;
+using rope::kI64;
+
+bool is_float(int32_t dt) { return dt == kF32 || dt == kF16 || dt == kBF16; }
+
+int64_t numel(const rope_tensor_t* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+bool shape_ok(const rope_tensor_t* t) {
+  if (t->ndim < 1 || t->ndim > 4) return false;
+  for (int i = 0; i < t->ndim; ++i)
+    if (t->shape[i] < 0) return false;
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t bytes) { return reinterpret_cast<uintptr_t>(p) % bytes == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? ROPE_OK : ROPE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int rope_inplace_partial(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_tensor_t* sin,
+                         int64_t rotary_mode, int64_t start, int64_t end, void* stream) {
+  if (!x || !cos || !sin) return ROPE_ERR_PARAM_NULLPTR;
+  // dtypes: x in {F32, F16, BF16}; cos == sin; cos == x, or F32 with a half x
+  if (!is_float(x->dtype) || !is_float(cos->dtype) || cos->dtype != sin->dtype) return ROPE_ERR_PARAM_INVALID;
+  if (cos->dtype != x->dtype && !(cos->dtype == kF32 && x->dtype != kF32)) return ROPE_ERR_PARAM_INVALID;
+  if (rotary_mode != 1) return ROPE_ERR_PARAM_INVALID;  // only interleave is open
+  if (x->ndim != 4 || cos->ndim != 4 || sin->ndim != 4) return ROPE_ERR_PARAM_INVALID;
+  if (!shape_ok(x) || !shape_ok(cos) || !shape_ok(sin)) return ROPE_ERR_PARAM_INVALID;
+  for (int i = 0; i < 4; ++i)
+    if (cos->shape[i] != sin->shape[i]) return ROPE_ERR_PARAM_INVALID;
+  const int64_t D = x->shape[3];
+  if (D > 1024 || D % 2) return ROPE_ERR_PARAM_INVALID;
+  if (start < 0 || end < 0 || end > D || start > end) return ROPE_ERR_PARAM_INVALID;
+  if (start == 0 && end == 0) end = D;  // no slice: the whole D axis
+  const int64_t L = end - start;
+  if (L % 2) return ROPE_ERR_PARAM_INVALID;
+  if (L == 0) return ROPE_OK;  // empty slice: no-op, nothing enqueued
+  if (cos->shape[3] != L) return ROPE_ERR_PARAM_INVALID;
+  for (int i = 0; i < 3; ++i)
+    if (cos->shape[i] != 1 && cos->shape[i] != x->shape[i]) return ROPE_ERR_PARAM_INVALID;
+  if (numel(x) == 0) return ROPE_OK;
+  if (!x->data || !cos->data || !sin->data) return ROPE_ERR_PARAM_NULLPTR;
+  const uintptr_t xe = x->dtype == kF32 ? 4 : 2, ce = cos->dtype == kF32 ? 4 : 2;
+  if (!aligned(x->data, xe) || !aligned(cos->data, ce) || !aligned(sin->data, ce)) return ROPE_ERR_PARAM_INVALID;
+
+  rope::InplaceProblem p;
+  p.x = x->data;
+  p.cos = cos->data;
+  p.sin = sin->data;
+  p.x_dtype = x->dtype;
+  p.cs_dtype = cos->dtype;
+  p.B = x->shape[0];
+  p.S = x->shape[1];
+  p.N = x->shape[2];
+  p.D = D;
+  p.start = start;
+  p.L = L;
+  const int64_t cB = cos->shape[0], cS = cos->shape[1], cN = cos->shape[2];
+  p.cs_n = cN == 1 ? 0 : 1;
+  p.cs_s = cS == 1 ? 0 : cN;
+  p.cs_b = cB == 1 ? 0 : cS * cN;
+  return cuda_status(rope::launch_inplace(p, static_cast<cudaStream_t>(stream)));
+}
+
+int rope_with_sin_cos_cache(const rope_tensor_t* positions, const rope_tensor_t* query,
+                            const rope_tensor_t* key, const rope_tensor_t* cos_sin_cache,
+                            int64_t head_size, int64_t rotary_dim, int32_t is_neox,
+                            const int64_t* mrope_section, int64_t mrope_section_len, void* stream) {
+  if (!positions || !query || !key || !cos_sin_cache) return ROPE_ERR_PARAM_NULLPTR;
+  // dtypes: positions int64; query, key and cache the same floating type
+  if (positions->dtype != kI64 || !is_float(query->dtype)) return ROPE_ERR_PARAM_INVALID;
+  if (key->dtype != query->dtype || cos_sin_cache->dtype != query->dtype) return ROPE_ERR_PARAM_INVALID;
+  // shapes: query, key, cache 2-D and non-empty; same token count
+  if (query->ndim != 2 || key->ndim != 2 || cos_sin_cache->ndim != 2) return ROPE_ERR_PARAM_INVALID;
+  if (!shape_ok(query) || !shape_ok(key) || !shape_ok(cos_sin_cache) || !shape_ok(positions))
+    return ROPE_ERR_PARAM_INVALID;
+  if (numel(query) == 0 || numel(key) == 0 || numel(cos_sin_cache) == 0) return ROPE_ERR_PARAM_INVALID;
+  const int64_t T = query->shape[0];
+  if (key->shape[0] != T) return ROPE_ERR_PARAM_INVALID;
+  // head size and rotary dim: 64-byte multiples; R == cache width <= head size
+  const int64_t mult = query->dtype == kF32 ? 16 : 32;
+  if (head_size <= 0 || head_size % mult) return ROPE_ERR_PARAM_INVALID;
+  if (query->shape[1] % head_size || key->shape[1] % head_size) return ROPE_ERR_PARAM_INVALID;
+  if (rotary_dim != cos_sin_cache->shape[1]) return ROPE_ERR_PARAM_INVALID;
+  if (rotary_dim <= 0 || rotary_dim % mult || rotary_dim > head_size) return ROPE_ERR_PARAM_INVALID;
+  // mode and positions shape
+  const bool mrope = mrope_section != nullptr && mrope_section_len > 0 && mrope_section[0] > 0;
+  if (mrope_section != nullptr && mrope_section_len != 3 && mrope_section_len != 4) return ROPE_ERR_PARAM_INVALID;
+  int32_t section_end[4] = {0, 0, 0, 0};
+  if (mrope_section != nullptr) {
+    int64_t sum = 0;
+    for (int64_t i = 0; i < mrope_section_len; ++i) {
+      if (mrope_section[i] < 0) return ROPE_ERR_PARAM_INVALID;
+      sum += mrope_section[i];
+      section_end[i] = (int32_t)sum;
+    }
+    if (mrope && 2 * sum != rotary_dim) return ROPE_ERR_PARAM_INVALID;
+  }
+  if (mrope) {
+    if (positions->ndim != 2 || positions->shape[0] != mrope_section_len || positions->shape[1] != T)
+      return ROPE_ERR_PARAM_INVALID;
+  } else {
+    if (positions->ndim != 1 || positions->shape[0] != T) return ROPE_ERR_PARAM_INVALID;
+  }
+  if (!positions->data || !query->data || !key->data || !cos_sin_cache->data) return ROPE_ERR_PARAM_NULLPTR;
+  if (!aligned(positions->data, 8) || !aligned(query->data, 16) || !aligned(key->data, 16) ||
+      !aligned(cos_sin_cache->data, 16))
+    return ROPE_ERR_PARAM_INVALID;
+
+  rope::CacheProblem p;
+  p.positions = static_cast<const int64_t*>(positions->data);
+  p.query = query->data;
+  p.key = key->data;
+  p.cache = cos_sin_cache->data;
+  p.dtype = query->dtype;
+  p.T = T;
+  p.hq = query->shape[1] / head_size;
+  p.hk = key->shape[1] / head_size;
+  p.head_size = head_size;
+  p.rotary_dim = rotary_dim;
+  p.max_seq = cos_sin_cache->shape[0];
+  p.is_neox = is_neox != 0;
+  p.mrope_rows = mrope ? (int32_t)mrope_section_len : 0;
+  for (int i = 0; i < 4; ++i) p.section_end[i] = section_end[i];
+  // one team of threads must fit one block of the cache kernel
+  if (rope::cache_team_threads(p) > 256) return ROPE_ERR_PARAM_INVALID;
+  if (p.hq + p.hk > (int64_t)1 << 30 || head_size > (int64_t)1 << 30) return ROPE_ERR_PARAM_INVALID;
+  return cuda_status(rope::launch_cache(p, static_cast<cudaStream_t>(stream)));
+}
+
+int rope_get_device_error(void* stream, int32_t* code) {
+  if (!code) return ROPE_ERR_PARAM_NULLPTR;
+  uint32_t c = 0;
+  const cudaError_t e = rope::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &c);
+  *code = (int32_t)c;
+  return cuda_status(e);
+}
+
+const char* rope_status_string(int status) {
+  switch (status) {
+    case ROPE_OK:
+      return "ROPE_OK";
+    case ROPE_ERR_PARAM_NULLPTR:
+      return "ROPE_ERR_PARAM_NULLPTR: a required tensor or its data pointer is NULL";
+    case ROPE_ERR_PARAM_INVALID:
+      return "ROPE_ERR_PARAM_INVALID: unsupported dtype, shape, slice, mode, section or alignment";
+    case ROPE_ERR_CUDA:
+      return "ROPE_ERR_CUDA: the CUDA runtime rejected a launch or query";
+    default:
+      return "unknown status";
+  }
+}
+
+uint64_t rope_launch_count(void) { return rope::g_launches.load(std::memory_order_relaxed); }
+
+int rope_abi_version(void) { return ROPE_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,115 @@
+// Device-side building blocks shared by the RoPE kernels: element conversions,
+// vector loads/stores with cache policies, and the accurate two-term dot product.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <float.h>
+#include <stdint.h>
+
+namespace rope {
+
+// ---------------------------------------------------------------------------
+// Element conversions: every storage type is widened exactly to binary32 and
+// narrowed back with one round-to-nearest-even.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float widen(float v) { return v; }
+__device__ __forceinline__ float widen(__half v) { return __half2float(v); }
+__device__ __forceinline__ float widen(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T narrow(float v);
+template <>
+__device__ __forceinline__ float narrow<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half narrow<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 narrow<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------------------
+// a*b - c*d with relative error at most 2^-23 (Kahan's algorithm: the rounding
+// error of c*d is recovered exactly by an FMA and added back; bound from
+// Jeannerod, Louvet & Muller, "Further analysis of Kahan's algorithm for the
+// accurate computation of 2x2 determinants", Math. Comp. 82 (2013)).  When c*d
+// is not finite the error term is meaningless and the plain FMA result is the
+// IEEE answer.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float diff_of_products(float a, float b, float c, float d) {
+  const float w = __fmul_rn(c, d);
+  const float e = __fmaf_rn(-c, d, w);  // w - c*d, exact
+  const float f = __fmaf_rn(a, b, -w);  // a*b - w, one rounding
+  const float r = __fadd_rn(f, e);
+  return fabsf(e) <= FLT_MAX ? r : f;
+}
+
+// ---------------------------------------------------------------------------
+// A register array of N elements, aligned so that it can be moved in 16-byte
+// (or smaller power-of-two) pieces.
+// ---------------------------------------------------------------------------
+template <typename T, int N>
+struct alignas((N * sizeof(T)) >= 16 ? 16 : (N * sizeof(T))) Vec {
+  T e[N];
+};
+
+// Global -> registers.  STREAM: data touched once (evict-first in L1 and L2);
+// otherwise read-only data that other threads reuse (non-coherent path).
+template <bool STREAM, int BYTES>
+__device__ __forceinline__ void gload(void* dst, const void* src) {
+  if constexpr (BYTES >= 16) {
+    static_assert(BYTES % 16 == 0, "vector size");
+#pragma unroll
+    for (int k = 0; k < BYTES / 16; ++k) {
+      const uint4* s = static_cast<const uint4*>(src) + k;
+      static_cast<uint4*>(dst)[k] = STREAM ? __ldcs(s) : __ldg(s);
+    }
+  } else if constexpr (BYTES == 8) {
+    const uint2* s = static_cast<const uint2*>(src);
+    *static_cast<uint2*>(dst) = STREAM ? __ldcs(s) : __ldg(s);
+  } else if constexpr (BYTES == 4) {
+    const unsigned int* s = static_cast<const unsigned int*>(src);
+    *static_cast<unsigned int*>(dst) = STREAM ? __ldcs(s) : __ldg(s);
+  } else {
+    static_assert(BYTES == 2, "vector size");
+    const unsigned short* s = static_cast<const unsigned short*>(src);
+    *static_cast<unsigned short*>(dst) = STREAM ? __ldcs(s) : __ldg(s);
+  }
+}
+
+// Registers -> global, streaming (evict-first).
+template <int BYTES>
+__device__ __forceinline__ void gstore(void* dst, const void* src) {
+  if constexpr (BYTES >= 16) {
+#pragma unroll
+    for (int k = 0; k < BYTES / 16; ++k)
+      __stcs(static_cast<uint4*>(dst) + k, static_cast<const uint4*>(src)[k]);
+  } else if constexpr (BYTES == 8) {
+    __stcs(static_cast<uint2*>(dst), *static_cast<const uint2*>(src));
+  } else if constexpr (BYTES == 4) {
+    __stcs(static_cast<unsigned int*>(dst), *static_cast<const unsigned int*>(src));
+  } else {
+    static_assert(BYTES == 2, "vector size");
+    __stcs(static_cast<unsigned short*>(dst), *static_cast<const unsigned short*>(src));
+  }
+}
+
+template <bool STREAM, typename T, int N>
+__device__ __forceinline__ void load_vec(Vec<T, N>& v, const T* p) {
+  gload<STREAM, N * sizeof(T)>(v.e, p);
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void store_vec(T* p, const Vec<T, N>& v) {
+  gstore<N * sizeof(T)>(p, v.e);
+}
+
+// Read-only vector load widened to binary32.
+template <typename T, int N>
+__device__ __forceinline__ void load_f32(float (&out)[N], const T* p) {
+  Vec<T, N> v;
+  load_vec<false>(v, p);
+#pragma unroll
+  for (int i = 0; i < N; ++i) out[i] = widen(v.e[i]);
+}
+
+}  // namespace rope

@@ -1,0 +1,262 @@
+// In-place partial interleave RoPE on a BSND tensor.
+//
+// Operator: "CANN ops-transformer 的 aclnnInplacePartialRotaryMul 算子：Inplace
+// 部分旋转位置编码接口详解与实现剖析", sections 计算原理与公式 and
+// partial_slice 局部旋转机制.  For each row r = (b, s, n) and pair p of the
+// slice (j = start + 2p), with cos/sin broadcast into r':
+//   x[r, j]   <- x[r, j]   * cos[r', 2p]   - x[r, j+1] * sin[r', 2p]
+//   x[r, j+1] <- x[r, j+1] * cos[r', 2p+1] + x[r, j]   * sin[r', 2p+1]
+//
+// GB300 design.  The work is HBM-bound (about 3 flops per 4-8 bytes), so the
+// kernel is organised around memory: a "team" of threads owns one token (b, s)
+// and a block of its heads; thread c of the team owns the c-th VEC-element
+// chunk of the slice (16-byte accesses when the slice is aligned).  When
+// cos/sin are broadcast over N (the usual [B|1, S, 1, L] layout) the thread
+// loads its cos/sin chunk once and keeps it in registers for every head of the
+// block; loads of U heads are issued before any compute so that each thread has
+// U independent 16-byte reads in flight.  x is read and written once with
+// evict-first (streaming) accesses; cos/sin use the read-only path and stay in
+// L2 for the other tokens that share them.  Columns outside the slice are never
+// touched.  A slice whose start is odd cannot be paired within an aligned
+// vector and takes a scalar pair-per-thread kernel instead.
+#include <algorithm>
+
+#include "rope_device.cuh"
+#include "rope_launch.h"
+
+namespace rope {
+namespace {
+
+constexpr int kHeadsInFlight = 4;  // U: heads loaded before compute, per thread
+
+struct InplaceArgs {
+  int64_t S, N, D;
+  int64_t start, L;
+  int64_t cs_b, cs_s, cs_n;
+  int64_t items;       // tokens * head_blocks
+  int32_t chunks;      // threads per team = L / VEC
+  int32_t heads_per_item;
+  int32_t head_blocks;
+};
+
+// Rotate VEC/2 interleaved pairs held in xv with per-element cos/sin.
+template <typename TX, int VEC>
+__device__ __forceinline__ void rotate_interleaved_pairs(Vec<TX, VEC>& xv, const float (&c)[VEC],
+                                                         const float (&s)[VEC]) {
+#pragma unroll
+  for (int q = 0; q < VEC / 2; ++q) {
+    const float x0 = widen(xv.e[2 * q]);
+    const float x1 = widen(xv.e[2 * q + 1]);
+    const float y0 = diff_of_products(x0, c[2 * q], x1, s[2 * q]);
+    const float y1 = diff_of_products(x1, c[2 * q + 1], -x0, s[2 * q + 1]);
+    xv.e[2 * q] = narrow<TX>(y0);
+    xv.e[2 * q + 1] = narrow<TX>(y1);
+  }
+}
+
+// PER_HEAD_CS: cos/sin carry their own row for every head (cN == N); otherwise
+// one cos/sin row serves all heads of the token.
+template <typename TX, typename TC, int VEC, bool PER_HEAD_CS>
+__global__ void __launch_bounds__(512) inplace_vec_kernel(TX* __restrict__ x, const TC* __restrict__ cosp,
+                                                          const TC* __restrict__ sinp, InplaceArgs a) {
+  constexpr int U = PER_HEAD_CS ? 2 : kHeadsInFlight;
+  const int team_size = a.chunks;
+  const int teams = blockDim.x / team_size;
+  const int team = threadIdx.x / team_size;
+  if (team >= teams) return;
+  const int c = threadIdx.x - team * team_size;
+  const int64_t team_stride = (int64_t)gridDim.x * teams;
+
+  for (int64_t item = (int64_t)blockIdx.x * teams + team; item < a.items; item += team_stride) {
+    const int64_t token = item / a.head_blocks;
+    const int hb = (int)(item - token * a.head_blocks);
+    const int64_t b = token / a.S;
+    const int64_t s = token - b * a.S;
+    const int h0 = hb * a.heads_per_item;
+    const int h1 = min(h0 + a.heads_per_item, (int)a.N);
+    TX* row = x + (token * a.N + h0) * a.D + a.start + (int64_t)c * VEC;
+    const int64_t coff = (b * a.cs_b + s * a.cs_s) * a.L + (int64_t)c * VEC;
+
+    if constexpr (!PER_HEAD_CS) {
+      // one cos/sin chunk serves every head of the block
+      float cf[VEC], sf[VEC];
+      load_f32<TC, VEC>(cf, cosp + coff);
+      load_f32<TC, VEC>(sf, sinp + coff);
+      for (int h = h0; h < h1; h += U, row += U * a.D) {
+        Vec<TX, VEC> xv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (h + u < h1) load_vec<true>(xv[u], row + u * a.D);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (h + u < h1) {
+            rotate_interleaved_pairs<TX, VEC>(xv[u], cf, sf);
+            store_vec(row + u * a.D, xv[u]);
+          }
+      }
+    } else {
+      // cos/sin vary with the head: one chunk per row
+      for (int h = h0; h < h1; h += U, row += U * a.D) {
+        Vec<TX, VEC> xv[U];
+        Vec<TC, VEC> cv[U], sv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (h + u < h1) {
+            const int64_t o = coff + (int64_t)(h + u) * a.cs_n * a.L;
+            load_vec<true>(xv[u], row + u * a.D);
+            load_vec<false>(cv[u], cosp + o);
+            load_vec<false>(sv[u], sinp + o);
+          }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (h + u < h1) {
+            float cf[VEC], sf[VEC];
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+              cf[i] = widen(cv[u].e[i]);
+              sf[i] = widen(sv[u].e[i]);
+            }
+            rotate_interleaved_pairs<TX, VEC>(xv[u], cf, sf);
+            store_vec(row + u * a.D, xv[u]);
+          }
+      }
+    }
+  }
+}
+
+// Fallback for slices that cannot be vectorised (odd start or misaligned
+// base): one thread per (row, pair), scalar accesses.
+template <typename TX, typename TC>
+__global__ void __launch_bounds__(256) inplace_pair_kernel(TX* __restrict__ x, const TC* __restrict__ cosp,
+                                                           const TC* __restrict__ sinp, InplaceArgs a,
+                                                           int64_t rows) {
+  const int64_t pairs = a.L / 2;
+  const int64_t total = rows * pairs;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / pairs;
+    const int64_t q = i - r * pairs;
+    const int64_t n = r % a.N;
+    const int64_t token = r / a.N;
+    const int64_t b = token / a.S;
+    const int64_t s = token - b * a.S;
+    const int64_t co = (b * a.cs_b + s * a.cs_s + n * a.cs_n) * a.L + 2 * q;
+    TX* p = x + r * a.D + a.start + 2 * q;
+    const float x0 = widen(p[0]);
+    const float x1 = widen(p[1]);
+    const float c0 = widen(cosp[co]), c1 = widen(cosp[co + 1]);
+    const float s0 = widen(sinp[co]), s1 = widen(sinp[co + 1]);
+    p[0] = narrow<TX>(diff_of_products(x0, c0, x1, s0));
+    p[1] = narrow<TX>(diff_of_products(x1, c1, -x0, s1));
+  }
+}
+
+bool aligned(const void* p, int64_t bytes) { return (reinterpret_cast<uintptr_t>(p) % bytes) == 0; }
+
+template <typename TX, typename TC, int VEC>
+cudaError_t launch_vec(const InplaceProblem& p, cudaStream_t stream) {
+  InplaceArgs a;
+  a.S = p.S;
+  a.N = p.N;
+  a.D = p.D;
+  a.start = p.start;
+  a.L = p.L;
+  a.cs_b = p.cs_b;
+  a.cs_s = p.cs_s;
+  a.cs_n = p.cs_n;
+  a.chunks = (int32_t)(p.L / VEC);
+  const int threads = a.chunks > 256 ? a.chunks : 256;
+  const int teams = threads / a.chunks;
+  // Split the heads of a token into blocks only when the tokens alone would not
+  // give each SM about a thousand threads.
+  const int64_t tokens = p.B * p.S;
+  const int64_t sms = sm_count();
+  const int64_t want_threads = sms * 1024;
+  const int64_t base_threads = tokens * a.chunks;
+  int64_t nb = (want_threads + base_threads - 1) / base_threads;
+  nb = std::max<int64_t>(1, std::min<int64_t>(nb, p.N));
+  a.heads_per_item = (int32_t)((p.N + nb - 1) / nb);
+  a.head_blocks = (int32_t)((p.N + a.heads_per_item - 1) / a.heads_per_item);
+  a.items = tokens * a.head_blocks;
+  const int64_t ctas_needed = (a.items + teams - 1) / teams;
+  const int64_t ctas_resident = sms * std::max(1, 2048 / threads);
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min(ctas_needed, ctas_resident));
+  if (p.cs_n == 0)
+    inplace_vec_kernel<TX, TC, VEC, false><<<grid, threads, 0, stream>>>(
+        static_cast<TX*>(p.x), static_cast<const TC*>(p.cos), static_cast<const TC*>(p.sin), a);
+  else
+    inplace_vec_kernel<TX, TC, VEC, true><<<grid, threads, 0, stream>>>(
+        static_cast<TX*>(p.x), static_cast<const TC*>(p.cos), static_cast<const TC*>(p.sin), a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <typename TX, typename TC>
+cudaError_t launch_pairs(const InplaceProblem& p, cudaStream_t stream) {
+  InplaceArgs a{};
+  a.S = p.S;
+  a.N = p.N;
+  a.D = p.D;
+  a.start = p.start;
+  a.L = p.L;
+  a.cs_b = p.cs_b;
+  a.cs_s = p.cs_s;
+  a.cs_n = p.cs_n;
+  const int64_t rows = p.B * p.S * p.N;
+  const int64_t total = rows * (p.L / 2);
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)sm_count() * 8);
+  inplace_pair_kernel<TX, TC><<<(unsigned)std::max<int64_t>(1, blocks), 256, 0, stream>>>(
+      static_cast<TX*>(p.x), static_cast<const TC*>(p.cos), static_cast<const TC*>(p.sin), a, rows);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// Widest vector (in elements of TX) that the slice, the row pitch and the
+// base pointers all allow; 0 when pairs cannot be kept inside one vector.
+template <typename TX, typename TC>
+int pick_vec(const InplaceProblem& p) {
+  const int max_vec = 16 / (int)sizeof(TX);
+  for (int v = max_vec; v >= 2; v /= 2) {
+    if (p.start % v || p.L % v || p.D % v) continue;
+    if (!aligned(p.x, v * (int64_t)sizeof(TX))) continue;
+    const int64_t cbytes = std::min<int64_t>(16, v * (int64_t)sizeof(TC));
+    if (!aligned(p.cos, cbytes) || !aligned(p.sin, cbytes)) continue;
+    return v;
+  }
+  return 0;
+}
+
+template <typename TX, typename TC>
+cudaError_t dispatch(const InplaceProblem& p, cudaStream_t stream) {
+  switch (pick_vec<TX, TC>(p)) {
+    case 8:
+      if constexpr (sizeof(TX) == 2) return launch_vec<TX, TC, 8>(p, stream);
+      break;
+    case 4:
+      return launch_vec<TX, TC, 4>(p, stream);
+    case 2:
+      return launch_vec<TX, TC, 2>(p, stream);
+    default:
+      break;
+  }
+  return launch_pairs<TX, TC>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_inplace(const InplaceProblem& p, cudaStream_t stream) {
+  const bool f32cs = p.cs_dtype == kF32;
+  switch (p.x_dtype) {
+    case kF32:
+      return dispatch<float, float>(p, stream);
+    case kF16:
+      return f32cs ? dispatch<__half, float>(p, stream) : dispatch<__half, __half>(p, stream);
+    case kBF16:
+      return f32cs ? dispatch<__nv_bfloat16, float>(p, stream)
+                   : dispatch<__nv_bfloat16, __nv_bfloat16>(p, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace rope
