@@ -7,9 +7,11 @@
 // runs on the host before anything is enqueued, and no check touches the GPU,
 // so a rejected call has no side effect at all.
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <tuple>
 
-#include "../../include/rope_gb300.h"
+#include "rope_gb300.h"
 #include "rope_launch.h"
 
 namespace rope {
@@ -32,6 +34,27 @@ int sm_count() {
     g_sm_count[dev] = n;
   });
   return g_sm_count[dev];
+}
+
+int resident_blocks(const void* kernel, int threads) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  const auto key = std::make_tuple(dev, kernel, threads);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();  // do not leave a sticky-looking error for the launch check
+    n = 1;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = n;
+  return n;
 }
 
 }  // namespace rope
@@ -172,7 +195,7 @@ int rope_with_sin_cos_cache(const rope_tensor_t* positions, const rope_tensor_t*
   p.mrope_rows = mrope ? (int32_t)mrope_section_len : 0;
   for (int i = 0; i < 4; ++i) p.section_end[i] = section_end[i];
   // one team of threads must fit one block of the cache kernel
-  if (rope::cache_team_threads(p) > 256) return ROPE_ERR_PARAM_INVALID;
+  if (rope::cache_team_threads(p) > rope::cache_max_team_threads()) return ROPE_ERR_PARAM_INVALID;
   if (p.hq + p.hk > (int64_t)1 << 30 || head_size > (int64_t)1 << 30) return ROPE_ERR_PARAM_INVALID;
   return cuda_status(rope::launch_cache(p, static_cast<cudaStream_t>(stream)));
 }

@@ -5,15 +5,18 @@
 // chunk, rotate), mrope 模式, rope 模式, rotate_half（GPT-NeoX style） and
 // rotate_interleaved（GPT-J style）.
 //
-// GB300 design.  Token-major teams, as in the in-place kernel: a team owns one
-// token and a block of its heads (query heads first, then key heads); thread c
-// owns one 16-byte chunk of cos and the matching chunk of sin.  The gather of
-// the cache row (mrope: the section's row for each owned index) happens once
-// per team, into registers, and serves every head of the block.  NeoX pairs
-// element i with i + R/2, so a thread loads the same chunk of both halves;
-// GPT-J pairs neighbours, so a thread loads one chunk holding VEC/2 pairs.
-// query/key are read and written once (streaming); the cache goes through the
-// read-only path and stays in L2 for later tokens at nearby positions.
+// GB300 design.  The work is a stream of "head rows" (token t, head h) over
+// the query heads then the key heads of each token, R rotated elements each,
+// cut into items of U consecutive heads of one token.  A CTA's P row groups (C
+// threads each) take P consecutive items and the persistent grid strides over
+// the items, so at any moment the whole GPU works inside a window of a few MB
+// of q/k: good DRAM row-buffer locality.  Thread c of a group owns one 16-byte
+// chunk of a row (NeoX: the same chunk of both halves, GPT-J: VEC/2
+// neighbouring pairs) and the matching cos/sin elements, gathered once per
+// item (mrope: spliced from the section rows) and kept in registers for its U
+// rows.  All U row loads are issued before the gather and any arithmetic, so
+// each thread keeps U (NeoX: 2U) 16-byte streaming reads in flight.  q/k are read and written once with evict-first
+// accesses; the cache goes through the read-only path and stays in L2.
 // Columns [R, head_size) of every head are never touched.
 //
 // A position outside [0, maxSeqLen) leaves its token untouched and sets bit
@@ -31,19 +34,29 @@ __device__ unsigned int g_device_error;
 
 namespace {
 
-constexpr int kHeadsInFlight = 4;  // U: heads loaded before compute, per thread
+// Compile-time launch parameters (the defaults are the measured best on GB300).
+#ifndef ROPE_CACHE_ROWS_IN_FLIGHT
+#define ROPE_CACHE_ROWS_IN_FLIGHT 4
+#endif
+#ifndef ROPE_CACHE_MIN_BLOCKS
+#define ROPE_CACHE_MIN_BLOCKS 1
+#endif
+#ifndef ROPE_CACHE_THREADS
+#define ROPE_CACHE_THREADS 256
+#endif
+constexpr int kRowsInFlight = ROPE_CACHE_ROWS_IN_FLIGHT;  // U: rows loaded before compute, per thread
+constexpr int kThreads = ROPE_CACHE_THREADS;
 constexpr unsigned kPositionOutOfRange = 1u;
 
 struct CacheArgs {
   int64_t T;
   int64_t max_seq;
-  int64_t items;  // T * head_blocks
+  int64_t items;       // T * head_chunks
+  int32_t head_chunks;  // ceil((hq + hk) / U): chunks of U consecutive heads per token
   int32_t hq, hk;
   int32_t head_size;
   int32_t R;
-  int32_t chunks;  // threads per team
-  int32_t heads_per_item;
-  int32_t head_blocks;
+  int32_t chunks;  // threads per row (C)
   int32_t mrope_rows;
   int32_t section_end[4];
 };
@@ -59,114 +72,114 @@ __device__ __forceinline__ int64_t select_row(int k, int64_t p0, int64_t p1, int
   return k == 0 ? p0 : k == 1 ? p1 : k == 2 ? p2 : p3;
 }
 
+// Steps 1-2 for one token: gather cosSin = cache[positions[t]] and split it
+// into this thread's NC cos and NC sin values (first owned index i0).
+// Returns false (nothing loaded) when a position is outside [0, maxSeqLen).
+template <typename T, int NC>
+__device__ __forceinline__ bool gather_cos_sin(const int64_t* __restrict__ pos, const T* __restrict__ cache,
+                                               const CacheArgs& a, int64_t t, int i0, float (&cf)[NC],
+                                               float (&sf)[NC]) {
+  const int half = a.R / 2;
+  if (a.mrope_rows == 0) {
+    const int64_t p = __ldg(pos + t);
+    if (p < 0 || p >= a.max_seq) return false;
+    const T* rowp = cache + p * a.R;
+    load_f32<T, NC>(cf, rowp + i0);
+    load_f32<T, NC>(sf, rowp + half + i0);
+    return true;
+  }
+  const int64_t p0 = __ldg(pos + t);
+  const int64_t p1 = __ldg(pos + a.T + t);
+  const int64_t p2 = __ldg(pos + 2 * a.T + t);
+  const int64_t p3 = a.mrope_rows > 3 ? __ldg(pos + 3 * a.T + t) : 0;
+  if (p0 < 0 || p0 >= a.max_seq || p1 < 0 || p1 >= a.max_seq || p2 < 0 || p2 >= a.max_seq || p3 < 0 ||
+      p3 >= a.max_seq)
+    return false;
+  const int k0 = section_of(i0, a);
+  const int k1 = section_of(i0 + NC - 1, a);
+  if (k0 == k1) {  // the whole chunk sits in one section: one vector per half
+    const T* rowp = cache + select_row(k0, p0, p1, p2, p3) * a.R;
+    load_f32<T, NC>(cf, rowp + i0);
+    load_f32<T, NC>(sf, rowp + half + i0);
+  } else {  // the chunk straddles a section boundary: per-element rows
+#pragma unroll
+    for (int e = 0; e < NC; ++e) {
+      const T* rowp = cache + select_row(section_of(i0 + e, a), p0, p1, p2, p3) * a.R;
+      cf[e] = widen(__ldg(rowp + i0 + e));
+      sf[e] = widen(__ldg(rowp + half + i0 + e));
+    }
+  }
+  return true;
+}
+
 template <typename T, bool NEOX, int VEC>
-__global__ void __launch_bounds__(256) cache_kernel(const int64_t* __restrict__ pos, T* __restrict__ q,
-                                                    T* __restrict__ k, const T* __restrict__ cache,
-                                                    CacheArgs a) {
-  constexpr int U = kHeadsInFlight;
+__global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
+    cache_kernel(const int64_t* __restrict__ pos, T* __restrict__ q, T* __restrict__ k,
+                 const T* __restrict__ cache, CacheArgs a) {
+  constexpr int U = kRowsInFlight;
   constexpr int NC = NEOX ? VEC : VEC / 2;  // cos (and sin) indices owned per thread
-  const int team_size = a.chunks;
-  const int teams = blockDim.x / team_size;
-  const int team = threadIdx.x / team_size;
-  if (team >= teams) return;
-  const int c = threadIdx.x - team * team_size;
+  const int C = a.chunks;
+  const int P = blockDim.x / C;  // row groups per CTA
+  const int g = threadIdx.x / C;
+  if (g >= P) return;
+  const int c = threadIdx.x - g * C;
   const int half = a.R / 2;
   const int i0 = c * NC;  // first owned cos index
-  const int64_t team_stride = (int64_t)gridDim.x * teams;
+  const int heads = a.hq + a.hk;
+  wait_for_prior_grid();
 
-  for (int64_t item = (int64_t)blockIdx.x * teams + team; item < a.items; item += team_stride) {
-    const int64_t t = item / a.head_blocks;
-    const int hb = (int)(item - t * a.head_blocks);
-
-    // ---- steps 1-2: gather cosSin = cache[positions] and split into cos / sin
-    float cf[NC], sf[NC];
-    bool ok = true;
-    if (a.mrope_rows == 0) {
-      const int64_t p = __ldg(pos + t);
-      ok = p >= 0 && p < a.max_seq;
-      if (ok) {
-        const T* rowp = cache + p * a.R;
-        load_f32<T, NC>(cf, rowp + i0);
-        load_f32<T, NC>(sf, rowp + half + i0);
-      }
-    } else {
-      const int64_t p0 = __ldg(pos + t);
-      const int64_t p1 = __ldg(pos + a.T + t);
-      const int64_t p2 = __ldg(pos + 2 * a.T + t);
-      const int64_t p3 = a.mrope_rows > 3 ? __ldg(pos + 3 * a.T + t) : 0;
-      ok = p0 >= 0 && p0 < a.max_seq && p1 >= 0 && p1 < a.max_seq && p2 >= 0 && p2 < a.max_seq &&
-           p3 >= 0 && p3 < a.max_seq;
-      if (ok) {
-        const int k0 = section_of(i0, a);
-        const int k1 = section_of(i0 + NC - 1, a);
-        if (k0 == k1) {  // the whole chunk sits in one section: one vector per half
-          const T* rowp = cache + select_row(k0, p0, p1, p2, p3) * a.R;
-          load_f32<T, NC>(cf, rowp + i0);
-          load_f32<T, NC>(sf, rowp + half + i0);
-        } else {  // chunk straddles a section boundary: per-element rows
+  // item = (token t, head chunk j): heads [j*U, min(j*U + U, heads)) of token t
+  for (int64_t item = (int64_t)blockIdx.x * P + g; item < a.items; item += (int64_t)gridDim.x * P) {
+    const int64_t t = item / a.head_chunks;
+    const int h0 = (int)(item - t * a.head_chunks) * U;
+    const int n = min(U, heads - h0);
+    // ---- issue the loads of the chunk's rows
+    T* base[U];
+    Vec<T, VEC> x1[U], x2[U];  // GPT-J uses x1 only
 #pragma unroll
-          for (int e = 0; e < NC; ++e) {
-            const T* rowp = cache + select_row(section_of(i0 + e, a), p0, p1, p2, p3) * a.R;
-            cf[e] = widen(__ldg(rowp + i0 + e));
-            sf[e] = widen(__ldg(rowp + half + i0 + e));
-          }
+    for (int u = 0; u < U; ++u) {
+      const int h = h0 + (u < n ? u : 0);
+      base[u] = h < a.hq ? q + (t * a.hq + h) * (int64_t)a.head_size
+                         : k + (t * a.hk + (h - a.hq)) * (int64_t)a.head_size;
+      if (u < n) {
+        if constexpr (NEOX) {
+          load_vec<true>(x1[u], base[u] + i0);
+          load_vec<true>(x2[u], base[u] + half + i0);
+        } else {
+          load_vec<true>(x1[u], base[u] + 2 * i0);
         }
       }
     }
-    if (!ok) {
-      if (c == 0 && hb == 0) atomicOr(&g_device_error, kPositionOutOfRange);
-      continue;
+    // ---- steps 1-2: the token's cos/sin chunk
+    float cf[NC], sf[NC];
+    if (!gather_cos_sin<T, NC>(pos, cache, a, t, i0, cf, sf)) {
+      // reported once per token, by thread 0 of the group holding head 0
+      if (c == 0 && h0 == 0) atomicOr(&g_device_error, kPositionOutOfRange);
+      continue;  // leave the token untouched
     }
-
-    // ---- step 3: rotate the first R columns of every head of the block
-    const int h0 = hb * a.heads_per_item;
-    const int h1 = min(h0 + a.heads_per_item, a.hq + a.hk);
-    for (int h = h0; h < h1; h += U) {
-      T* base[U];
+    // ---- step 3: rotate and store
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int hh = h + u < h1 ? h + u : h;
-        base[u] = hh < a.hq ? q + (t * a.hq + hh) * (int64_t)a.head_size
-                            : k + (t * a.hk + (hh - a.hq)) * (int64_t)a.head_size;
-      }
+    for (int u = 0; u < U; ++u) {
+      if (u >= n) break;
       if constexpr (NEOX) {
-        Vec<T, VEC> x1[U], x2[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (h + u < h1) {
-            load_vec<true>(x1[u], base[u] + i0);
-            load_vec<true>(x2[u], base[u] + half + i0);
-          }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (h + u < h1) {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              const float a1 = widen(x1[u].e[e]);
-              const float a2 = widen(x2[u].e[e]);
-              x1[u].e[e] = narrow<T>(diff_of_products(a1, cf[e], a2, sf[e]));
-              x2[u].e[e] = narrow<T>(diff_of_products(a2, cf[e], -a1, sf[e]));
-            }
-            store_vec(base[u] + i0, x1[u]);
-            store_vec(base[u] + half + i0, x2[u]);
-          }
+        for (int e = 0; e < VEC; ++e) {
+          const float a1 = widen(x1[u].e[e]);
+          const float a2 = widen(x2[u].e[e]);
+          x1[u].e[e] = narrow<T>(diff_of_products(a1, cf[e], a2, sf[e]));
+          x2[u].e[e] = narrow<T>(diff_of_products(a2, cf[e], -a1, sf[e]));
+        }
+        store_vec(base[u] + i0, x1[u]);
+        store_vec(base[u] + half + i0, x2[u]);
       } else {
-        Vec<T, VEC> xv[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (h + u < h1) load_vec<true>(xv[u], base[u] + 2 * i0);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (h + u < h1) {
-#pragma unroll
-            for (int e = 0; e < NC; ++e) {
-              const float a1 = widen(xv[u].e[2 * e]);
-              const float a2 = widen(xv[u].e[2 * e + 1]);
-              xv[u].e[2 * e] = narrow<T>(diff_of_products(a1, cf[e], a2, sf[e]));
-              xv[u].e[2 * e + 1] = narrow<T>(diff_of_products(a2, cf[e], -a1, sf[e]));
-            }
-            store_vec(base[u] + 2 * i0, xv[u]);
-          }
+        for (int e = 0; e < NC; ++e) {
+          const float a1 = widen(x1[u].e[2 * e]);
+          const float a2 = widen(x1[u].e[2 * e + 1]);
+          x1[u].e[2 * e] = narrow<T>(diff_of_products(a1, cf[e], a2, sf[e]));
+          x1[u].e[2 * e + 1] = narrow<T>(diff_of_products(a2, cf[e], -a1, sf[e]));
+        }
+        store_vec(base[u] + 2 * i0, x1[u]);
       }
     }
   }
@@ -186,25 +199,17 @@ cudaError_t launch_typed(const CacheProblem& p, cudaStream_t stream) {
   a.mrope_rows = p.mrope_rows;
   // ends past the used sections are R/2, so section_of() never counts them
   for (int i = 0; i < 4; ++i) a.section_end[i] = i < p.mrope_rows ? p.section_end[i] : (int32_t)(p.rotary_dim / 2);
-  const int threads = a.chunks > 256 ? a.chunks : 256;
-  const int teams = threads / a.chunks;
-  const int64_t heads = p.hq + p.hk;
-  const int64_t sms = sm_count();
-  const int64_t want_threads = sms * 1024;
-  const int64_t base_threads = p.T * a.chunks;
-  int64_t nb = (want_threads + base_threads - 1) / base_threads;
-  nb = std::max<int64_t>(1, std::min<int64_t>(nb, heads));
-  a.heads_per_item = (int32_t)((heads + nb - 1) / nb);
-  a.head_blocks = (int32_t)((heads + a.heads_per_item - 1) / a.heads_per_item);
-  a.items = p.T * a.head_blocks;
-  const int64_t ctas_needed = (a.items + teams - 1) / teams;
-  const int64_t ctas_resident = sms * std::max(1, 2048 / threads);
-  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min(ctas_needed, ctas_resident));
-  cache_kernel<T, NEOX, VEC><<<grid, threads, 0, stream>>>(p.positions, static_cast<T*>(p.query),
-                                                           static_cast<T*>(p.key),
-                                                           static_cast<const T*>(p.cache), a);
-  count_launch();
-  return cudaGetLastError();
+  a.head_chunks = (int32_t)((p.hq + p.hk + kRowsInFlight - 1) / kRowsInFlight);
+  a.items = p.T * a.head_chunks;
+  const int threads = kThreads;
+  const int64_t groups = threads / a.chunks;
+  // Persistent grid: the CTAs that fit on the GPU at once stride over the items,
+  // P consecutive items per CTA per step.
+  const void* kfn = reinterpret_cast<const void*>(cache_kernel<T, NEOX, VEC>);
+  const int64_t resident = (int64_t)sm_count() * resident_blocks(kfn, threads);
+  const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
+  return launch_overlapped(cache_kernel<T, NEOX, VEC>, (unsigned)grid, threads, stream, p.positions,
+                           static_cast<T*>(p.query), static_cast<T*>(p.key), static_cast<const T*>(p.cache), a);
 }
 
 template <typename T>
@@ -218,6 +223,8 @@ int64_t cache_team_threads(const CacheProblem& p) {
   const int64_t vec = 16 / (p.dtype == kF32 ? 4 : 2);
   return p.is_neox ? (p.rotary_dim / 2) / vec : p.rotary_dim / vec;
 }
+
+int64_t cache_max_team_threads() { return kThreads; }
 
 cudaError_t launch_cache(const CacheProblem& p, cudaStream_t stream) {
   switch (p.dtype) {

@@ -10,6 +10,11 @@
 
 namespace rope {
 
+// Wait until the grid this kernel depends on (the previous kernel of the
+// stream, when launched with programmatic stream serialization) has completed
+// and its memory is visible; returns at once otherwise.
+__device__ __forceinline__ void wait_for_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Element conversions: every storage type is widened exactly to binary32 and
 // narrowed back with one round-to-nearest-even.

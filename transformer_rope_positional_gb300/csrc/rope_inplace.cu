@@ -8,17 +8,20 @@
 //   x[r, j+1] <- x[r, j+1] * cos[r', 2p+1] + x[r, j]   * sin[r', 2p+1]
 //
 // GB300 design.  The work is HBM-bound (about 3 flops per 4-8 bytes), so the
-// kernel is organised around memory: a "team" of threads owns one token (b, s)
-// and a block of its heads; thread c of the team owns the c-th VEC-element
-// chunk of the slice (16-byte accesses when the slice is aligned).  When
-// cos/sin are broadcast over N (the usual [B|1, S, 1, L] layout) the thread
-// loads its cos/sin chunk once and keeps it in registers for every head of the
-// block; loads of U heads are issued before any compute so that each thread has
-// U independent 16-byte reads in flight.  x is read and written once with
-// evict-first (streaming) accesses; cos/sin use the read-only path and stay in
-// L2 for the other tokens that share them.  Columns outside the slice are never
-// touched.  A slice whose start is odd cannot be paired within an aligned
-// vector and takes a scalar pair-per-thread kernel instead.
+// kernel is organised around memory.  The rows (b, s, n) of x form one
+// stream, cut into items of U consecutive heads of one token.  A CTA's P row
+// groups (C threads each) take P consecutive items and the persistent grid
+// strides over the items, so the whole GPU works inside a window of a few MB at
+// any moment (good DRAM row-buffer locality).  Thread c of a group owns the
+// c-th VEC-element chunk of the slice (16-byte accesses when the slice is
+// aligned).  When cos/sin are broadcast over N (the usual [B|1, S, 1, L]
+// layout) the item's rows share one cos/sin chunk, loaded once into registers;
+// otherwise every row loads its own chunk alongside x.  All U row loads are
+// issued before any arithmetic.  x is read and written once with evict-first
+// (streaming) accesses; cos/sin use the read-only path and stay in L2 for the
+// other tokens that share them.  Columns outside the slice are never touched.
+// A slice whose start is odd cannot be paired within an aligned vector and
+// takes a scalar pair-per-thread kernel instead.
 #include <algorithm>
 
 #include "rope_device.cuh"
@@ -27,16 +30,26 @@
 namespace rope {
 namespace {
 
-constexpr int kHeadsInFlight = 4;  // U: heads loaded before compute, per thread
+// Compile-time launch parameters (the defaults are the measured best on GB300).
+#ifndef ROPE_INPLACE_ROWS_IN_FLIGHT
+#define ROPE_INPLACE_ROWS_IN_FLIGHT 4
+#endif
+#ifndef ROPE_INPLACE_THREADS
+#define ROPE_INPLACE_THREADS 256
+#endif
+#ifndef ROPE_INPLACE_MIN_BLOCKS
+#define ROPE_INPLACE_MIN_BLOCKS 1
+#endif
+constexpr int kRowsInFlight = ROPE_INPLACE_ROWS_IN_FLIGHT;  // U: rows loaded before compute, per thread
+constexpr int kThreads = ROPE_INPLACE_THREADS;
 
 struct InplaceArgs {
   int64_t S, N, D;
   int64_t start, L;
   int64_t cs_b, cs_s, cs_n;
-  int64_t items;       // tokens * head_blocks
-  int32_t chunks;      // threads per team = L / VEC
-  int32_t heads_per_item;
-  int32_t head_blocks;
+  int64_t items;        // B * S * head_chunks
+  int32_t head_chunks;  // ceil(N / U): chunks of U consecutive heads per token
+  int32_t chunks;       // threads per row = L / VEC
 };
 
 // Rotate VEC/2 interleaved pairs held in xv with per-element cos/sin.
@@ -57,68 +70,61 @@ __device__ __forceinline__ void rotate_interleaved_pairs(Vec<TX, VEC>& xv, const
 // PER_HEAD_CS: cos/sin carry their own row for every head (cN == N); otherwise
 // one cos/sin row serves all heads of the token.
 template <typename TX, typename TC, int VEC, bool PER_HEAD_CS>
-__global__ void __launch_bounds__(512) inplace_vec_kernel(TX* __restrict__ x, const TC* __restrict__ cosp,
-                                                          const TC* __restrict__ sinp, InplaceArgs a) {
-  constexpr int U = PER_HEAD_CS ? 2 : kHeadsInFlight;
-  const int team_size = a.chunks;
-  const int teams = blockDim.x / team_size;
-  const int team = threadIdx.x / team_size;
-  if (team >= teams) return;
-  const int c = threadIdx.x - team * team_size;
-  const int64_t team_stride = (int64_t)gridDim.x * teams;
+__global__ void __launch_bounds__(512, ROPE_INPLACE_MIN_BLOCKS)
+    inplace_vec_kernel(TX* __restrict__ x, const TC* __restrict__ cosp, const TC* __restrict__ sinp,
+                       InplaceArgs a) {
+  constexpr int U = kRowsInFlight;
+  const int C = a.chunks;
+  const int P = blockDim.x / C;  // row groups per CTA
+  const int g = threadIdx.x / C;
+  if (g >= P) return;
+  const int c = threadIdx.x - g * C;
+  wait_for_prior_grid();
 
-  for (int64_t item = (int64_t)blockIdx.x * teams + team; item < a.items; item += team_stride) {
-    const int64_t token = item / a.head_blocks;
-    const int hb = (int)(item - token * a.head_blocks);
-    const int64_t b = token / a.S;
-    const int64_t s = token - b * a.S;
-    const int h0 = hb * a.heads_per_item;
-    const int h1 = min(h0 + a.heads_per_item, (int)a.N);
-    TX* row = x + (token * a.N + h0) * a.D + a.start + (int64_t)c * VEC;
-    const int64_t coff = (b * a.cs_b + s * a.cs_s) * a.L + (int64_t)c * VEC;
-
-    if constexpr (!PER_HEAD_CS) {
-      // one cos/sin chunk serves every head of the block
+  // item = (token t, head chunk j): heads [j*U, min(j*U + U, N)) of token t
+  for (int64_t item = (int64_t)blockIdx.x * P + g; item < a.items; item += (int64_t)gridDim.x * P) {
+    const int64_t t = item / a.head_chunks;
+    const int h0 = (int)(item - t * a.head_chunks) * U;
+    const int n = min(U, (int)a.N - h0);
+    TX* xrow = x + (t * a.N + h0) * a.D + a.start + (int64_t)c * VEC;
+    const int64_t b = t / a.S;
+    const int64_t coff = (b * a.cs_b + (t - b * a.S) * a.cs_s) * a.L + (int64_t)c * VEC;
+    // ---- issue the loads of the item's rows (and, per head, of their cos/sin)
+    Vec<TX, VEC> xv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (u < n) load_vec<true>(xv[u], xrow + u * a.D);
+    if constexpr (PER_HEAD_CS) {
+      Vec<TC, VEC> cv[U], sv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (u < n) {
+          const int64_t o = coff + (int64_t)(h0 + u) * a.cs_n * a.L;
+          load_vec<false>(cv[u], cosp + o);
+          load_vec<false>(sv[u], sinp + o);
+        }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (u >= n) break;
+        float cf[VEC], sf[VEC];
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+          cf[i] = widen(cv[u].e[i]);
+          sf[i] = widen(sv[u].e[i]);
+        }
+        rotate_interleaved_pairs<TX, VEC>(xv[u], cf, sf);
+        store_vec(xrow + u * a.D, xv[u]);
+      }
+    } else {
+      // one cos/sin chunk serves the item's heads
       float cf[VEC], sf[VEC];
       load_f32<TC, VEC>(cf, cosp + coff);
       load_f32<TC, VEC>(sf, sinp + coff);
-      for (int h = h0; h < h1; h += U, row += U * a.D) {
-        Vec<TX, VEC> xv[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (h + u < h1) load_vec<true>(xv[u], row + u * a.D);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (h + u < h1) {
-            rotate_interleaved_pairs<TX, VEC>(xv[u], cf, sf);
-            store_vec(row + u * a.D, xv[u]);
-          }
-      }
-    } else {
-      // cos/sin vary with the head: one chunk per row
-      for (int h = h0; h < h1; h += U, row += U * a.D) {
-        Vec<TX, VEC> xv[U];
-        Vec<TC, VEC> cv[U], sv[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (h + u < h1) {
-            const int64_t o = coff + (int64_t)(h + u) * a.cs_n * a.L;
-            load_vec<true>(xv[u], row + u * a.D);
-            load_vec<false>(cv[u], cosp + o);
-            load_vec<false>(sv[u], sinp + o);
-          }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (h + u < h1) {
-            float cf[VEC], sf[VEC];
-#pragma unroll
-            for (int i = 0; i < VEC; ++i) {
-              cf[i] = widen(cv[u].e[i]);
-              sf[i] = widen(sv[u].e[i]);
-            }
-            rotate_interleaved_pairs<TX, VEC>(xv[u], cf, sf);
-            store_vec(row + u * a.D, xv[u]);
-          }
+      for (int u = 0; u < U; ++u) {
+        if (u >= n) break;
+        rotate_interleaved_pairs<TX, VEC>(xv[u], cf, sf);
+        store_vec(xrow + u * a.D, xv[u]);
       }
     }
   }
@@ -132,6 +138,7 @@ __global__ void __launch_bounds__(256) inplace_pair_kernel(TX* __restrict__ x, c
                                                            int64_t rows) {
   const int64_t pairs = a.L / 2;
   const int64_t total = rows * pairs;
+  wait_for_prior_grid();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / pairs;
@@ -153,8 +160,8 @@ __global__ void __launch_bounds__(256) inplace_pair_kernel(TX* __restrict__ x, c
 
 bool aligned(const void* p, int64_t bytes) { return (reinterpret_cast<uintptr_t>(p) % bytes) == 0; }
 
-template <typename TX, typename TC, int VEC>
-cudaError_t launch_vec(const InplaceProblem& p, cudaStream_t stream) {
+template <typename TX, typename TC, int VEC, bool PER_HEAD_CS>
+cudaError_t launch_vec_kernel(const InplaceProblem& p, cudaStream_t stream) {
   InplaceArgs a;
   a.S = p.S;
   a.N = p.N;
@@ -165,30 +172,24 @@ cudaError_t launch_vec(const InplaceProblem& p, cudaStream_t stream) {
   a.cs_s = p.cs_s;
   a.cs_n = p.cs_n;
   a.chunks = (int32_t)(p.L / VEC);
-  const int threads = a.chunks > 256 ? a.chunks : 256;
-  const int teams = threads / a.chunks;
-  // Split the heads of a token into blocks only when the tokens alone would not
-  // give each SM about a thousand threads.
-  const int64_t tokens = p.B * p.S;
-  const int64_t sms = sm_count();
-  const int64_t want_threads = sms * 1024;
-  const int64_t base_threads = tokens * a.chunks;
-  int64_t nb = (want_threads + base_threads - 1) / base_threads;
-  nb = std::max<int64_t>(1, std::min<int64_t>(nb, p.N));
-  a.heads_per_item = (int32_t)((p.N + nb - 1) / nb);
-  a.head_blocks = (int32_t)((p.N + a.heads_per_item - 1) / a.heads_per_item);
-  a.items = tokens * a.head_blocks;
-  const int64_t ctas_needed = (a.items + teams - 1) / teams;
-  const int64_t ctas_resident = sms * std::max(1, 2048 / threads);
-  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min(ctas_needed, ctas_resident));
-  if (p.cs_n == 0)
-    inplace_vec_kernel<TX, TC, VEC, false><<<grid, threads, 0, stream>>>(
-        static_cast<TX*>(p.x), static_cast<const TC*>(p.cos), static_cast<const TC*>(p.sin), a);
-  else
-    inplace_vec_kernel<TX, TC, VEC, true><<<grid, threads, 0, stream>>>(
-        static_cast<TX*>(p.x), static_cast<const TC*>(p.cos), static_cast<const TC*>(p.sin), a);
-  count_launch();
-  return cudaGetLastError();
+  a.head_chunks = (int32_t)((p.N + kRowsInFlight - 1) / kRowsInFlight);
+  a.items = p.B * p.S * a.head_chunks;
+  // a row group needs C threads: the block has at least kThreads and at least C
+  const int threads = a.chunks > kThreads ? a.chunks : kThreads;
+  const int64_t groups = threads / a.chunks;
+  // Persistent grid: the CTAs that fit on the GPU at once stride over the items,
+  // P consecutive items per CTA per step.
+  auto kernel = inplace_vec_kernel<TX, TC, VEC, PER_HEAD_CS>;
+  const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), threads);
+  const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
+  return launch_overlapped(kernel, (unsigned)grid, threads, stream, static_cast<TX*>(p.x),
+                           static_cast<const TC*>(p.cos), static_cast<const TC*>(p.sin), a);
+}
+
+template <typename TX, typename TC, int VEC>
+cudaError_t launch_vec(const InplaceProblem& p, cudaStream_t stream) {
+  return p.cs_n == 0 ? launch_vec_kernel<TX, TC, VEC, false>(p, stream)
+                     : launch_vec_kernel<TX, TC, VEC, true>(p, stream);
 }
 
 template <typename TX, typename TC>
@@ -205,10 +206,9 @@ cudaError_t launch_pairs(const InplaceProblem& p, cudaStream_t stream) {
   const int64_t rows = p.B * p.S * p.N;
   const int64_t total = rows * (p.L / 2);
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)sm_count() * 8);
-  inplace_pair_kernel<TX, TC><<<(unsigned)std::max<int64_t>(1, blocks), 256, 0, stream>>>(
-      static_cast<TX*>(p.x), static_cast<const TC*>(p.cos), static_cast<const TC*>(p.sin), a, rows);
-  count_launch();
-  return cudaGetLastError();
+  return launch_overlapped(inplace_pair_kernel<TX, TC>, (unsigned)std::max<int64_t>(1, blocks), 256, stream,
+                           static_cast<TX*>(p.x), static_cast<const TC*>(p.cos), static_cast<const TC*>(p.sin), a,
+                           rows);
 }
 
 // Widest vector (in elements of TX) that the slice, the row pitch and the

@@ -42,8 +42,10 @@ struct CacheProblem {
 cudaError_t launch_inplace(const InplaceProblem& p, cudaStream_t stream);
 cudaError_t launch_cache(const CacheProblem& p, cudaStream_t stream);
 
-// Largest number of threads one team of the cache kernel may need.
+// Threads that work on one head row in the cache kernel, and the most a CTA
+// of that kernel holds.
 int64_t cache_team_threads(const CacheProblem& p);
+int64_t cache_max_team_threads();
 
 // Device error word of the current device.
 cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t* code);
@@ -51,5 +53,31 @@ cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t* code);
 // Launch bookkeeping.
 void count_launch();
 int sm_count();
+// CTAs of `kernel` (launched with `threads` threads, no dynamic shared memory)
+// that fit on one SM of the current device; cached, at least 1.
+int resident_blocks(const void* kernel, int threads);
+
+// Launch `kernel` on `stream` with programmatic stream serialization allowed:
+// the kernel may be scheduled while the previous kernel of the stream drains,
+// and every kernel of this library executes wait_for_prior_grid() before its
+// first global memory access, so stream order is unchanged; only the launch
+// latency is overlapped with the previous kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  count_launch();
+  return e == cudaSuccess ? cudaGetLastError() : e;
+}
 
 }  // namespace rope
