@@ -53,10 +53,10 @@ def _get_lib():
         lib.oracle_decode.restype = ctypes.c_double
         lib.oracle_encode.argtypes = [ctypes.c_double, ctypes.c_int]
         lib.oracle_encode.restype = ctypes.c_uint32
-        lib.oracle_inplace_partial_rotary_mul.argtypes = [
+        lib.oracle_inplace_partial_rope.argtypes = [
             ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-            ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
-        lib.oracle_inplace_partial_rotary_mul.restype = ctypes.c_int
+            ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+        lib.oracle_inplace_partial_rope.restype = ctypes.c_int
         lib.oracle_rope_with_sin_cos_cache.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
@@ -114,17 +114,21 @@ def round_to(values: np.ndarray, dtype: torch.dtype) -> torch.Tensor:
 
 
 def inplace_partial_rotary_mul(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
-                               start: int, end: int) -> torch.Tensor:
-    """Oracle of the in-place partial interleave operator; returns the new x."""
+                               start: int, end: int, rotary_mode: int = 1,
+                               backward: bool = False) -> torch.Tensor:
+    """Oracle of the in-place partial operator (mode 1 interleave, 0 half).
+
+    Forward returns the new x; ``backward=True`` treats ``x`` as dL/dy and
+    returns dL/dx."""
     out = _cpu(x).clone()
     c, s = _cpu(cos), _cpu(sin)
     assert out.dim() == 4 and c.dim() == 4 and tuple(c.shape) == tuple(s.shape)
-    assert c.dtype == s.dtype
+    assert c.dtype == s.dtype and rotary_mode in (0, 1)
     xs = (ctypes.c_int64 * 4)(*out.shape)
     cs = (ctypes.c_int64 * 4)(*c.shape)
-    rc = _get_lib().oracle_inplace_partial_rotary_mul(
+    rc = _get_lib().oracle_inplace_partial_rope(
         out.data_ptr(), _CODE[out.dtype], ctypes.addressof(xs), c.data_ptr(), s.data_ptr(),
-        _CODE[c.dtype], ctypes.addressof(cs), int(start), int(end))
+        _CODE[c.dtype], ctypes.addressof(cs), int(start), int(end), int(rotary_mode), 1 if backward else 0)
     if rc != 0:
         raise MemoryError("oracle allocation failed")
     return out

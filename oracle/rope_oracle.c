@@ -25,6 +25,8 @@
  *      of the two, flattened), so every pair (2p, 2p+1) is rotated on its own.
  *      cos and sin multiply element-wise (their last dim equals the slice
  *      length), so slot 2p+1 uses cos[2p+1] and sin[2p+1].
+ *      rotary_mode 0 ("half", declared by the page but not open there) is the
+ *      same formula with x1, x2 the two halves of the slice (rotate_half).
  *  (2) [IPRM §partial_slice 局部旋转机制]: slice [0,0] (or no slice) means the
  *      whole D axis; any other start == end is a no-op.
  *  (3) [IPRM §约束说明]: cos/sin broadcast against x per dim (each of B, S, N
@@ -137,27 +139,53 @@ double oracle_decode(uint32_t bits, int dt) { return decode_bits(bits, fmt_of(dt
 uint32_t oracle_encode(double v, int dt) { return encode_bits(v, fmt_of(dt)); }
 int oracle_elem_bytes(int dt) { return bytes_of(dt); }
 
+/* The rotated vector x_rotate of [IPRM §计算原理与公式] for one slice of
+ * length L.  mode 1 (interleave, reading (1)): slot 2p holds -v[2p+1] and slot
+ * 2p+1 holds v[2p].  mode 0 (half): the formula's cat(-x2, x1) taken with x1,
+ * x2 the two halves of the slice, i.e. rotate_half. */
+static void rotated_vector(const double* v, double* out, int64_t L, int mode) {
+  if (mode == 1) {
+    for (int64_t p = 0; p < L / 2; ++p) {
+      out[2 * p] = -v[2 * p + 1];
+      out[2 * p + 1] = v[2 * p];
+    }
+  } else {
+    for (int64_t i = 0; i < L / 2; ++i) {
+      out[i] = -v[L / 2 + i];
+      out[L / 2 + i] = v[i];
+    }
+  }
+}
+
 /*
- * In-place partial interleave rotary multiply.  [IPRM §计算原理与公式,
- * §partial_slice 局部旋转机制, §约束说明]
+ * In-place partial rotary multiply, forward or backward.
+ * [IPRM §计算原理与公式, §partial_slice 局部旋转机制, §约束说明,
+ *  §Python 接口与自动微分 (the backward op computes only x's gradient)]
  *
  * x:   [B, S, N, D] contiguous, type x_dt, rewritten in place on [start, end).
+ *      For the backward it holds dL/dy on entry and dL/dx on return.
  * cos, sin: [cB, cS, cN, L] contiguous, type cs_dt, L = end - start; each of
  *      cB, cS, cN is 1 (broadcast) or equal to x's.
- * Returns 0 (the caller validates shapes).
+ * mode: 1 interleave, 0 half.
+ * Forward:  y = x * cos + x_rotate * sin, element-wise.
+ * Backward: the transpose of that linear map.  x_rotate = P x with P
+ *      antisymmetric (P^T = -P), so dL/dx = dy * cos - P (dy * sin).
+ * Returns 0 (the caller validates shapes), -1 on allocation failure.
  */
-int oracle_inplace_partial_rotary_mul(void* x, int x_dt, const int64_t* x_shape, const void* cos,
-                                      const void* sin, int cs_dt, const int64_t* cs_shape,
-                                      int64_t start, int64_t end) {
+int oracle_inplace_partial_rope(void* x, int x_dt, const int64_t* x_shape, const void* cos, const void* sin,
+                                int cs_dt, const int64_t* cs_shape, int64_t start, int64_t end, int mode,
+                                int backward) {
   const int64_t B = x_shape[0], S = x_shape[1], N = x_shape[2], D = x_shape[3];
   if (start == 0 && end == 0) end = D; /* no slice: the whole D axis */
   if (start == end) return 0;          /* empty slice: no-op */
   const int64_t L = end - start;
   double* xs = (double*)malloc(sizeof(double) * (size_t)L);
   double* xrot = (double*)malloc(sizeof(double) * (size_t)L);
-  if (!xs || !xrot) {
+  double* tmp = (double*)malloc(sizeof(double) * (size_t)L);
+  if (!xs || !xrot || !tmp) {
     free(xs);
     free(xrot);
+    free(tmp);
     return -1;
   }
   for (int64_t b = 0; b < B; ++b)
@@ -170,21 +198,28 @@ int oracle_inplace_partial_rotary_mul(void* x, int x_dt, const int64_t* x_shape,
         const int64_t crow = ((cb * cs_shape[1] + cs) * cs_shape[2] + cn) * L;
         /* the rotated part x[..., start:end] */
         for (int64_t j = 0; j < L; ++j) xs[j] = load_elem(x, x_dt, xrow + start + j);
-        /* x1 = xs[0::2], x2 = xs[1::2]; rotated vector = (-x2, x1) pair by pair */
-        for (int64_t p = 0; p < L / 2; ++p) {
-          xrot[2 * p] = -xs[2 * p + 1];
-          xrot[2 * p + 1] = xs[2 * p];
-        }
-        /* x = x * cos + x_rotate * sin, element-wise */
-        for (int64_t j = 0; j < L; ++j) {
-          double c = load_elem(cos, cs_dt, crow + j);
-          double sn = load_elem(sin, cs_dt, crow + j);
-          double y = xs[j] * c + xrot[j] * sn;
-          store_elem(x, x_dt, xrow + start + j, y);
+        if (!backward) {
+          /* x = x * cos + x_rotate * sin, element-wise */
+          rotated_vector(xs, xrot, L, mode);
+          for (int64_t j = 0; j < L; ++j) {
+            double c = load_elem(cos, cs_dt, crow + j);
+            double sn = load_elem(sin, cs_dt, crow + j);
+            double y = xs[j] * c + xrot[j] * sn;
+            store_elem(x, x_dt, xrow + start + j, y);
+          }
+        } else {
+          /* dx = dy * cos - P (dy * sin) */
+          for (int64_t j = 0; j < L; ++j) tmp[j] = xs[j] * load_elem(sin, cs_dt, crow + j);
+          rotated_vector(tmp, xrot, L, mode);
+          for (int64_t j = 0; j < L; ++j) {
+            double dx = xs[j] * load_elem(cos, cs_dt, crow + j) - xrot[j];
+            store_elem(x, x_dt, xrow + start + j, dx);
+          }
         }
       }
   free(xs);
   free(xrot);
+  free(tmp);
   return 0;
 }
 

@@ -12,7 +12,15 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "rope_oracle.c")
 # (name, text in rope_oracle.c, replacement)
 MUTANTS = [
     ("interleave sign of the rotated odd member",
-     "xrot[2 * p] = -xs[2 * p + 1];", "xrot[2 * p] = xs[2 * p + 1];"),
+     "out[2 * p] = -v[2 * p + 1];", "out[2 * p] = v[2 * p + 1];"),
+    ("half mode: rotated halves swapped",
+     "out[i] = -v[L / 2 + i];\n      out[L / 2 + i] = v[i];", "out[i] = v[L / 2 + i];\n      out[L / 2 + i] = -v[i];"),
+    ("backward: sin applied after the rotation",
+     "for (int64_t j = 0; j < L; ++j) tmp[j] = xs[j] * load_elem(sin, cs_dt, crow + j);",
+     "for (int64_t j = 0; j < L; ++j) tmp[j] = xs[j] * load_elem(sin, cs_dt, crow + (j ^ 1));"),
+    ("backward: forward sign of the rotated term",
+     "double dx = xs[j] * load_elem(cos, cs_dt, crow + j) - xrot[j];",
+     "double dx = xs[j] * load_elem(cos, cs_dt, crow + j) + xrot[j];"),
     ("interleave sin element index",
      "double sn = load_elem(sin, cs_dt, crow + j);", "double sn = load_elem(sin, cs_dt, crow + (j ^ 1));"),
     ("interleave dropped sin term",

@@ -456,3 +456,130 @@ def test_special_values_propagate():
     # pair (inf, nan) and pair (1, 2)
     assert math.isnan(qo[0, 0]) and math.isnan(qo[0, 2])
     assert qo[0, 1].item() == 1.0 * 0.25 - 2.0 * 0.75 and qo[0, 3].item() == 2.0 * 0.25 + 1.0 * 0.75
+
+
+# ----------------------------------------------------------------------------
+# in-place operator: half mode (rotary_mode 0) and backward
+# ----------------------------------------------------------------------------
+
+def test_half_mode_and_backward_hand_cases():
+    g = _load("inplace_half_and_backward_hand_cases.json")
+
+    def t(v):
+        return torch.tensor(v, dtype=torch.float32).reshape(1, 1, 1, -1)
+
+    hf = g["half_forward"]
+    y = oracle.inplace_partial_rotary_mul(t(hf["x"]), t(hf["cos"]), t(hf["sin"]), 0, 0, rotary_mode=0)
+    assert y.reshape(-1).tolist() == hf["y"]
+    hb = g["half_backward"]
+    dx = oracle.inplace_partial_rotary_mul(t(hb["g"]), t(hb["cos"]), t(hb["sin"]), 0, 0, rotary_mode=0,
+                                           backward=True)
+    assert dx.reshape(-1).tolist() == hb["dx"]
+    ib = g["interleave_backward"]
+    dx = oracle.inplace_partial_rotary_mul(t(ib["g"]), t(ib["cos"]), t(ib["sin"]), 0, 0, rotary_mode=1,
+                                           backward=True)
+    assert dx.reshape(-1).tolist() == ib["dx"]
+
+
+def _half_rotation_tables(rows, L, base=10000.0):
+    """cos/sin for half mode: index i and i + L/2 share the angle rows*theta_i."""
+    i = np.arange(L) % (L // 2)
+    theta = base ** (-2.0 * i / L)
+    ang = np.arange(rows, dtype=np.float64)[:, None] * theta[None, :]
+    return np.cos(ang), np.sin(ang)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_half_mode_matches_complex_form(dt):
+    B, S, N, D, st, en = 2, 6, 3, 40, 8, 32
+    L = en - st
+    x = W.normal(77, (B, S, N, D), dt)
+    c, s = _half_rotation_tables(S, L)
+    cos = torch.from_numpy(c).float().to(dt).reshape(1, S, 1, L)
+    sin = torch.from_numpy(s).float().to(dt).reshape(1, S, 1, L)
+    y = oracle.inplace_partial_rotary_mul(x, cos, sin, st, en, rotary_mode=0)
+    xd = x.double().numpy().copy()
+    h = L // 2
+    z = xd[..., st:st + h] + 1j * xd[..., st + h:en]
+    w = np.broadcast_to(cos.double().numpy()[..., :h] + 1j * sin.double().numpy()[..., :h], z.shape)
+    r = z * w
+    xd[..., st:st + h] = r.real
+    xd[..., st + h:en] = r.imag
+    assert _ulp_dist(y, oracle.round_to(xd, dt)).max() <= 1
+
+
+def test_half_mode_equals_interleave_under_permutation():
+    """Half mode on the de-interleaved slice (evens, then odds) equals the
+    de-interleaved interleave-mode result, with cos/sin permuted the same way."""
+    case = W.inplace_case("perm", 78, (2, 5, 3, 32), 0, 32, torch.float32, torch.float32,
+                          cs_shape=(2, 5, 3, 32), cs_kind="randn")
+    perm = torch.cat([torch.arange(0, 32, 2), torch.arange(1, 32, 2)])
+    yi = oracle.inplace_partial_rotary_mul(case.x, case.cos, case.sin, 0, 32, rotary_mode=1)
+    yh = oracle.inplace_partial_rotary_mul(case.x[..., perm].contiguous(), case.cos[..., perm].contiguous(),
+                                           case.sin[..., perm].contiguous(), 0, 32, rotary_mode=0)
+    assert _same_bits(yh, yi[..., perm].contiguous())
+
+
+def _torch_forward(x, cos, sin, start, end, mode):
+    """The forward formula in torch float64 ops, for autograd."""
+    L = end - start
+    xs = x[..., start:end]
+    if mode == 1:
+        rot = torch.stack((-xs[..., 1::2], xs[..., 0::2]), dim=-1).reshape(xs.shape)
+    else:
+        rot = torch.cat((-xs[..., L // 2:], xs[..., :L // 2]), dim=-1)
+    y = x.clone()
+    y[..., start:end] = xs * cos + rot * sin
+    return y
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_backward_is_the_gradient_of_the_forward(mode, dt):
+    case = W.inplace_case("grad", 79, (2, 4, 3, 48), 8, 40, dt, torch.float32, cs_shape=(2, 4, 1, 32),
+                          cs_kind="randn")
+    gy = W.normal(80, case.x.shape, dt)
+    x = case.x.double().requires_grad_(True)
+    y = _torch_forward(x, case.cos.double(), case.sin.double(), 8, 40, mode)
+    (y * gy.double()).sum().backward()
+    ref = oracle.round_to(x.grad.numpy(), dt)
+    got = oracle.inplace_partial_rotary_mul(gy, case.cos, case.sin, 8, 40, rotary_mode=mode, backward=True)
+    assert _ulp_dist(got, ref).max() <= 1
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_backward_adjoint_identity(mode):
+    """<F x, g> == <x, F^T g> for random x, g and free cos/sin (float64 sums of
+    float32 results; the tolerance covers the two output roundings)."""
+    case = W.inplace_case("adj", 81, (3, 5, 2, 64), 0, 64, torch.float32, torch.float32, cs_shape=(3, 5, 2, 64),
+                          cs_kind="randn")
+    g = W.normal(82, case.x.shape, torch.float32)
+    fx = oracle.inplace_partial_rotary_mul(case.x, case.cos, case.sin, 0, 64, rotary_mode=mode).double()
+    ftg = oracle.inplace_partial_rotary_mul(g, case.cos, case.sin, 0, 64, rotary_mode=mode, backward=True).double()
+    lhs = float((fx * g.double()).sum())
+    rhs = float((case.x.double() * ftg).sum())
+    scale = float((fx.abs() * g.double().abs()).sum())
+    assert abs(lhs - rhs) <= 4 * 2.0 ** -24 * scale
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_backward_of_rotation_is_the_inverse_rotation(mode):
+    L = 32
+    if mode == 1:
+        case = W.inplace_f32_small("slice")
+        cos, sin = case.cos, case.sin
+    else:
+        c, s = _half_rotation_tables(16, L)
+        cos = torch.from_numpy(c).float().reshape(1, 16, 1, L)
+        sin = torch.from_numpy(s).float().reshape(1, 16, 1, L)
+    g = W.normal(83, (1, 16, 2, 64), torch.float32)
+    a = oracle.inplace_partial_rotary_mul(g, cos, sin, 16, 48, rotary_mode=mode, backward=True)
+    b = oracle.inplace_partial_rotary_mul(g, cos, -sin, 16, 48, rotary_mode=mode)
+    assert _same_bits(a, b)
+
+
+def test_backward_noop_and_untouched_columns():
+    case = W.inplace_case("bwd_noop", 84, (2, 3, 2, 32), 8, 24, torch.float16, torch.float32)
+    assert _same_bits(oracle.inplace_partial_rotary_mul(case.x, case.cos, case.sin, 8, 8, backward=True), case.x)
+    dx = oracle.inplace_partial_rotary_mul(case.x, case.cos, case.sin, 8, 24, backward=True)
+    assert _same_bits(dx[..., :8], case.x[..., :8]) and _same_bits(dx[..., 24:], case.x[..., 24:])
