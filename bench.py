@@ -289,6 +289,10 @@ def run_ours(args):
         ev[nk].record()
     torch.cuda.synchronize()
     per_kernel_ms = [[events[s_][i].elapsed_time(events[s_][i + 1]) for s_ in range(Kk)] for i in range(nk)]
+
+    # ---- rows beyond the hot path (backward, half mode), each timed cold: a
+    # large cache-op launch runs between two of them and flushes their data from L2
+    next_rows = time_next_rows(cases, dev_tensors, calls, Kk)
     sampler.stop()
     clocks = sampler.summary(t_host0, t_host1)
     ms_step_local = total_ms / K
@@ -330,12 +334,50 @@ def run_ours(args):
                            "l2": "inputs larger than L2: %.2f GB per step vs %d MB L2; each kernel's buffers are "
                                  "evicted by the others between its launches" % (total_bytes / 1e9, L2_BYTES >> 20),
                            "parallelism": "replicas of the per-GPU workload (weak scaling), no collective"},
-                "per_kernel": kernels, "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+                "per_kernel": kernels, "next_rows": next_rows, "roofline": roofline, "e2e": e2e,
+                "gpu_launches": launches,
                 "clocks": clocks, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def time_next_rows(cases, dev_tensors, calls, steps):
+    """Per-launch time of the in-place operator's backward (interleave) and of
+    its half mode on the [4,4096,32,128] workload.  Sequence per step:
+    backward, NeoX cache launch (flushes L2), half mode, mrope launch."""
+    import transformer_rope_positional_gb300 as R
+    c = cases[0]
+    x, cs, sn = dev_tensors[0]
+    extra = [("inplace_backward_interleave_" + c.name.split("_", 1)[1],
+              R.prepare_inplace_partial(x, cs, sn, 1, [c.start, c.end], backward=True)),
+             ("inplace_half_forward_" + c.name.split("_", 1)[1],
+              R.prepare_inplace_partial(x, cs, sn, 0, [c.start, c.end]))]
+    flushers = [calls[1], calls[3]]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for _ in range(3):
+        for (_, call), fl in zip(extra, flushers):
+            call()
+            fl()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(4e6))
+    for s_ in range(steps):
+        for i, ((_, call), fl) in enumerate(zip(extra, flushers)):
+            ev[s_][2 * i].record()
+            call()
+            ev[s_][2 * i + 1].record()
+            fl()
+    torch.cuda.synchronize()
+    peak, _ = measured_peak()
+    b = algorithmic_bytes(c)
+    out = []
+    for i, (name, _) in enumerate(extra):
+        ms = [ev[s_][2 * i].elapsed_time(ev[s_][2 * i + 1]) for s_ in range(steps)]
+        avg = sum(ms) / len(ms)
+        out.append({"workload": name, "bytes_per_launch": b, "launches": steps, "avg_us": round(avg * 1e3, 3),
+                    "gbs": round(b / (avg * 1e-3) / 1e9, 1), "frac_of_peak": round(b / (avg * 1e-3) / 1e9 / peak, 4)})
+    return out
 
 
 def run_e2e(args, cases, dev_tensors, calls, world, dev, total_bytes):

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define ROPE_ABI_VERSION 1
+#define ROPE_ABI_VERSION 2
 
 typedef enum {
   ROPE_F32 = 0,  /* IEEE binary32 */
@@ -74,22 +74,24 @@ enum {
 };
 
 /*
- * In-place partial interleave RoPE.
+ * In-place partial RoPE (interleave or half mode).
  * [IPRM §计算原理与公式, §partial_slice 局部旋转机制, §约束说明, §返回值与错误码]
  *
- * For every row r = (b, s, n) of x and every pair p of the slice (j = start + 2p):
- *     x[r, j]   <- x[r, j]   * cos[r', 2p]   - x[r, j+1] * sin[r', 2p]
- *     x[r, j+1] <- x[r, j+1] * cos[r', 2p+1] + x[r, j]   * sin[r', 2p+1]
- * (the page's  x = x*cos + x_rotate*sin  with x_rotate built pair by pair from
- * the negated odd member and the even member), where r' is r broadcast into
- * cos/sin's [cB, cS, cN] dims.  Columns outside [start, end) are never read
- * or written.
+ * For every row r = (b, s, n) of x and every pair of the slice -- slot j and its
+ * partner j', with j = start + 2p, j' = j + 1 in interleave mode (rotary_mode 1)
+ * and j = start + i, j' = j + L/2 in half mode (rotary_mode 0) --
+ *     x[r, j]  <- x[r, j]  * cos[r', j - start]  - x[r, j'] * sin[r', j - start]
+ *     x[r, j'] <- x[r, j'] * cos[r', j' - start] + x[r, j]  * sin[r', j' - start]
+ * (the page's  x = x*cos + x_rotate*sin  with x_rotate built from the negated
+ * partners; interleave is the mode the page opens, half -- rotate_half over the
+ * slice -- is the mode it declares), where r' is r broadcast into cos/sin's
+ * [cB, cS, cN] dims.  Columns outside [start, end) are never read or written.
  *
  *   x            [B, S, N, D]; F32, F16 or BF16; D even, D <= 1024.  Rewritten in place.
  *   cos, sin     [cB, cS, cN, L] with L = end - start; each of cB, cS, cN is 1 or
  *                equal to x's B, S, N.  Same dtype as x, or F32 when x is F16/BF16
  *                (computed in binary32, the page's mixed-precision combination).
- *   rotary_mode  must be 1 (interleave); 0 (half) is declared by the page but not open.
+ *   rotary_mode  1 (interleave) or 0 (half); other values are rejected.
  *   start, end   the slice [start, end) of the D axis.  [0, 0] means the whole axis;
  *                any other start == end is a no-op that enqueues nothing.
  *                0 <= start <= end <= D, and end - start even.
@@ -100,6 +102,21 @@ enum {
  */
 int rope_inplace_partial(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_tensor_t* sin,
                          int64_t rotary_mode, int64_t start, int64_t end, void* stream);
+
+/*
+ * Backward of rope_inplace_partial with respect to x, in place.
+ * [IPRM §Python 接口与自动微分: the backward op computes the gradient of x only
+ *  (cos/sin get none) and is a no-op for empty tensors and empty slices]
+ *
+ * `grad` holds dL/dy on entry and dL/dx on return.  Per pair (j, j') as above:
+ *     grad[r, j]  <- grad[r, j]  * cos[r', j - start]  + grad[r, j'] * sin[r', j' - start]
+ *     grad[r, j'] <- grad[r, j'] * cos[r', j' - start] - grad[r, j]  * sin[r', j - start]
+ * i.e. the transpose of the forward map (for a true rotation, the inverse
+ * rotation).  Arguments, checks and status values are those of
+ * rope_inplace_partial, with `grad` in the place of x.
+ */
+int rope_inplace_partial_backward(const rope_tensor_t* grad, const rope_tensor_t* cos, const rope_tensor_t* sin,
+                                  int64_t rotary_mode, int64_t start, int64_t end, void* stream);
 
 /*
  * Cache-indexed RoPE of query and key, in place.

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.rope_abi_version() == 1
+    assert lib.rope_abi_version() == 2
     for st in (C.ROPE_OK, C.ROPE_ERR_PARAM_NULLPTR, C.ROPE_ERR_PARAM_INVALID, C.ROPE_ERR_CUDA, 12345):
         s = C.status_string(st)
         assert isinstance(s, str) and s
@@ -84,9 +84,27 @@ def test_inplace_dtype_rules(lib, xdt, cdt, sdt, ok):
     assert st == (C.ROPE_OK if ok else C.ROPE_ERR_PARAM_INVALID)
 
 
-@pytest.mark.parametrize("mode", [0, 2, 3, -1])
-def test_inplace_only_interleave_mode(lib, mode):
+@pytest.mark.parametrize("mode", [2, 3, -1, 4])
+def test_inplace_modes_without_a_formula_rejected(lib, mode):
+    # 0 (half) and 1 (interleave) are accepted; QUARTER (2), DEEPSEEK_INTERLEAVE (3)
+    # and anything else have no formula on the page
     assert _inplace(lib, _d(C.F32, X), _d(C.F32, CS), _d(C.F32, CS), mode=mode) == C.ROPE_ERR_PARAM_INVALID
+
+
+def _backward(lib, x, c, s, mode=1, start=0, end=0):
+    return lib.rope_inplace_partial_backward(ctypes.byref(x) if x else None, ctypes.byref(c) if c else None,
+                                             ctypes.byref(s) if s else None, mode, start, end, None)
+
+
+def test_backward_shares_the_forward_checks(lib):
+    assert _backward(lib, None, _d(C.F32, CS), _d(C.F32, CS)) == C.ROPE_ERR_PARAM_NULLPTR
+    assert _backward(lib, _d(C.F32, X), _d(C.F16, CS), _d(C.F16, CS)) == C.ROPE_ERR_PARAM_INVALID
+    assert _backward(lib, _d(C.F32, X), _d(C.F32, CS), _d(C.F32, CS), mode=2) == C.ROPE_ERR_PARAM_INVALID
+    assert _backward(lib, _d(C.F32, X), _d(C.F32, (1, 3, 1, 8)), _d(C.F32, (1, 3, 1, 8)), start=0,
+                     end=16) == C.ROPE_ERR_PARAM_INVALID
+    before = lib.rope_launch_count()
+    assert _backward(lib, _d(C.F32, X), _d(C.F32, CS), _d(C.F32, CS), start=8, end=8) == C.ROPE_OK
+    assert lib.rope_launch_count() == before
 
 
 @pytest.mark.parametrize("xs,cs,start,end", [

@@ -75,3 +75,22 @@ def test_gptj_f16_partial_workload_full_size(rope_gpu):
 
 def test_mrope_workload_full_size(rope_gpu):
     _check_cache_sampled(W.mrope_neox_bf16(), 104)
+
+
+@pytest.mark.parametrize("run", [("half", False), ("interleave", True)], ids=["half_fwd", "interleave_bwd"])
+def test_mixed_bf16_workload_full_size_other_modes(rope_gpu, run):
+    mode, backward = run
+    case = W.inplace_bf16_mixed()
+    x = case.x.cuda()
+    fn = R.rope_inplace_partial_backward if backward else R.rope_inplace_partial
+    fn(x, case.cos.cuda(), case.sin.cuda(), mode, [case.start, case.end])
+    got = x.cpu()
+    B, S, N, D = case.x.shape
+    assert same_bits(got[..., :64], case.x[..., :64])
+    for t in _sample(B * S, 105).tolist():
+        b, s = divmod(t, S)
+        ref = oracle.inplace_partial_rotary_mul(case.x[b:b + 1, s:s + 1].contiguous(),
+                                                case.cos[:, s:s + 1].contiguous(), case.sin[:, s:s + 1].contiguous(),
+                                                case.start, case.end, rotary_mode=R._capi.MODES[mode],
+                                                backward=backward)
+        assert_matches(got[b:b + 1, s:s + 1], ref, "token %d" % t)

@@ -24,12 +24,17 @@ from ._capi import (  # noqa: F401
     prepare_inplace_partial,
     prepare_with_sin_cos_cache,
     rope_inplace_partial,
+    rope_inplace_partial_backward,
     rope_with_sin_cos_cache,
     status_string,
 )
 
+from .autograd import inplace_partial_rotary_mul  # noqa: E402,F401
+
 __all__ = [
+    "inplace_partial_rotary_mul",
     "rope_inplace_partial",
+    "rope_inplace_partial_backward",
     "rope_with_sin_cos_cache",
     "get_device_error",
     "launch_count",

@@ -25,7 +25,8 @@ ROPE_ERR_PARAM_INVALID = 161002
 ROPE_ERR_CUDA = 561000
 ROPE_DEVICE_POSITION_OUT_OF_RANGE = 1
 
-EXPORTED = ("rope_inplace_partial", "rope_with_sin_cos_cache", "rope_get_device_error",
+EXPORTED = ("rope_inplace_partial", "rope_inplace_partial_backward", "rope_with_sin_cos_cache",
+            "rope_get_device_error",
             "rope_status_string", "rope_launch_count", "rope_abi_version")
 
 
@@ -57,6 +58,8 @@ def load() -> ctypes.CDLL:
     lib.rope_inplace_partial.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_void_p]
     lib.rope_inplace_partial.restype = ctypes.c_int
+    lib.rope_inplace_partial_backward.argtypes = lib.rope_inplace_partial.argtypes
+    lib.rope_inplace_partial_backward.restype = ctypes.c_int
     lib.rope_with_sin_cos_cache.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                             ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_void_p]
     lib.rope_with_sin_cos_cache.restype = ctypes.c_int
@@ -104,22 +107,51 @@ def _stream_handle(t: torch.Tensor, stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def rope_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode: int = 1,
-                         partial_slice: Optional[Sequence[int]] = None, stream=None) -> None:
-    """In-place partial interleave RoPE of ``x`` [B, S, N, D] over ``partial_slice``.
+MODES = {"interleave": 1, "half": 0, 1: 1, 0: 0}
 
-    ``partial_slice=None`` means ``[0, 0]``, the whole D axis.  Returns None; x
-    is rewritten on ``stream`` (default: the current stream of x's device).
+
+def _mode(rotary_mode) -> int:
+    if rotary_mode not in MODES:
+        raise RopeError(ROPE_ERR_PARAM_INVALID, "rotary_mode %r" % (rotary_mode,))
+    return MODES[rotary_mode]
+
+
+def _slice(partial_slice):
+    if partial_slice is None:
+        return 0, 0
+    if len(partial_slice) != 2:
+        raise RopeError(ROPE_ERR_PARAM_INVALID, "partial_slice must have two elements")
+    return int(partial_slice[0]), int(partial_slice[1])
+
+
+def rope_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode=1,
+                         partial_slice: Optional[Sequence[int]] = None, stream=None) -> None:
+    """In-place partial RoPE of ``x`` [B, S, N, D] over ``partial_slice``.
+
+    ``rotary_mode``: 1 / "interleave" or 0 / "half".  ``partial_slice=None``
+    means ``[0, 0]``, the whole D axis.  Returns None; x is rewritten on
+    ``stream`` (default: the current stream of x's device).
     """
-    start, end = (0, 0) if partial_slice is None else (int(partial_slice[0]), int(partial_slice[1]))
-    if partial_slice is not None and len(partial_slice) != 2:
-        raise RopeError(ROPE_ERR_PARAM_INVALID, "rope_inplace_partial")
+    start, end = _slice(partial_slice)
     lib = load()
     dx, dc, ds = tensor_desc(x), tensor_desc(cos), tensor_desc(sin)
-    st = lib.rope_inplace_partial(ctypes.byref(dx), ctypes.byref(dc), ctypes.byref(ds), int(rotary_mode),
+    st = lib.rope_inplace_partial(ctypes.byref(dx), ctypes.byref(dc), ctypes.byref(ds), _mode(rotary_mode),
                                   start, end, _stream_handle(x, stream))
     if st != ROPE_OK:
         raise RopeError(st, "rope_inplace_partial")
+
+
+def rope_inplace_partial_backward(grad: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode=1,
+                                  partial_slice: Optional[Sequence[int]] = None, stream=None) -> None:
+    """Backward of :func:`rope_inplace_partial`: turns dL/dy in ``grad`` into
+    dL/dx in place."""
+    start, end = _slice(partial_slice)
+    lib = load()
+    dg, dc, ds = tensor_desc(grad), tensor_desc(cos), tensor_desc(sin)
+    st = lib.rope_inplace_partial_backward(ctypes.byref(dg), ctypes.byref(dc), ctypes.byref(ds),
+                                           _mode(rotary_mode), start, end, _stream_handle(grad, stream))
+    if st != ROPE_OK:
+        raise RopeError(st, "rope_inplace_partial_backward")
 
 
 def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: torch.Tensor,
@@ -179,14 +211,17 @@ class PreparedCall:
             raise RopeError(st, self._what)
 
 
-def prepare_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode: int = 1,
-                            partial_slice: Optional[Sequence[int]] = None, stream=None) -> PreparedCall:
+def prepare_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode=1,
+                            partial_slice: Optional[Sequence[int]] = None, stream=None,
+                            backward: bool = False) -> PreparedCall:
     lib = load()
-    start, end = (0, 0) if partial_slice is None else (int(partial_slice[0]), int(partial_slice[1]))
+    start, end = _slice(partial_slice)
     dx, dc, ds = tensor_desc(x), tensor_desc(cos), tensor_desc(sin)
-    args = (ctypes.byref(dx), ctypes.byref(dc), ctypes.byref(ds), int(rotary_mode), start, end,
+    args = (ctypes.byref(dx), ctypes.byref(dc), ctypes.byref(ds), _mode(rotary_mode), start, end,
             _stream_handle(x, stream))
-    return PreparedCall(lib.rope_inplace_partial, args, (x, cos, sin, dx, dc, ds), "rope_inplace_partial")
+    fn = lib.rope_inplace_partial_backward if backward else lib.rope_inplace_partial
+    return PreparedCall(fn, args, (x, cos, sin, dx, dc, ds),
+                        "rope_inplace_partial_backward" if backward else "rope_inplace_partial")
 
 
 def prepare_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: torch.Tensor,

@@ -85,17 +85,15 @@ bool aligned(const void* p, uintptr_t bytes) { return reinterpret_cast<uintptr_t
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? ROPE_OK : ROPE_ERR_CUDA; }
 
-}  // namespace
-
-extern "C" {
-
-int rope_inplace_partial(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_tensor_t* sin,
-                         int64_t rotary_mode, int64_t start, int64_t end, void* stream) {
+// Checks shared by the forward and backward in-place calls, then the launch.
+int inplace_call(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_tensor_t* sin, int64_t rotary_mode,
+                 int64_t start, int64_t end, bool backward, void* stream) {
   if (!x || !cos || !sin) return ROPE_ERR_PARAM_NULLPTR;
   // dtypes: x in {F32, F16, BF16}; cos == sin; cos == x, or F32 with a half x
   if (!is_float(x->dtype) || !is_float(cos->dtype) || cos->dtype != sin->dtype) return ROPE_ERR_PARAM_INVALID;
   if (cos->dtype != x->dtype && !(cos->dtype == kF32 && x->dtype != kF32)) return ROPE_ERR_PARAM_INVALID;
-  if (rotary_mode != 1) return ROPE_ERR_PARAM_INVALID;  // only interleave is open
+  // modes: 1 interleave, 0 half; the other enum values have no formula
+  if (rotary_mode != 1 && rotary_mode != 0) return ROPE_ERR_PARAM_INVALID;
   if (x->ndim != 4 || cos->ndim != 4 || sin->ndim != 4) return ROPE_ERR_PARAM_INVALID;
   if (!shape_ok(x) || !shape_ok(cos) || !shape_ok(sin)) return ROPE_ERR_PARAM_INVALID;
   for (int i = 0; i < 4; ++i)
@@ -116,6 +114,8 @@ int rope_inplace_partial(const rope_tensor_t* x, const rope_tensor_t* cos, const
   if (!aligned(x->data, xe) || !aligned(cos->data, ce) || !aligned(sin->data, ce)) return ROPE_ERR_PARAM_INVALID;
 
   rope::InplaceProblem p;
+  p.mode = (int32_t)rotary_mode;
+  p.backward = backward;
   p.x = x->data;
   p.cos = cos->data;
   p.sin = sin->data;
@@ -132,6 +132,20 @@ int rope_inplace_partial(const rope_tensor_t* x, const rope_tensor_t* cos, const
   p.cs_s = cS == 1 ? 0 : cN;
   p.cs_b = cB == 1 ? 0 : cS * cN;
   return cuda_status(rope::launch_inplace(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int rope_inplace_partial(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_tensor_t* sin,
+                         int64_t rotary_mode, int64_t start, int64_t end, void* stream) {
+  return inplace_call(x, cos, sin, rotary_mode, start, end, false, stream);
+}
+
+int rope_inplace_partial_backward(const rope_tensor_t* grad, const rope_tensor_t* cos, const rope_tensor_t* sin,
+                                  int64_t rotary_mode, int64_t start, int64_t end, void* stream) {
+  return inplace_call(grad, cos, sin, rotary_mode, start, end, true, stream);
 }
 
 int rope_with_sin_cos_cache(const rope_tensor_t* positions, const rope_tensor_t* query,

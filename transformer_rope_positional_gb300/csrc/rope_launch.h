@@ -9,8 +9,10 @@ namespace rope {
 
 enum DType : int32_t { kF32 = 0, kF16 = 1, kBF16 = 2, kI64 = 3 };
 
-// In-place partial interleave RoPE on x[B, S, N, D], slice [start, start + L).
+// In-place partial RoPE on x[B, S, N, D], slice [start, start + L).
 struct InplaceProblem {
+  int32_t mode;   // 1 interleave, 0 half
+  bool backward;  // apply the transpose (gradient) instead of the forward map
   void* x;
   const void* cos;
   const void* sin;
@@ -39,7 +41,11 @@ struct CacheProblem {
   int32_t section_end[4];  // cumulative ends of the mrope sections (cos indices)
 };
 
-cudaError_t launch_inplace(const InplaceProblem& p, cudaStream_t stream);
+cudaError_t launch_inplace_forward(const InplaceProblem& p, cudaStream_t stream);
+cudaError_t launch_inplace_backward(const InplaceProblem& p, cudaStream_t stream);
+inline cudaError_t launch_inplace(const InplaceProblem& p, cudaStream_t stream) {
+  return p.backward ? launch_inplace_backward(p, stream) : launch_inplace_forward(p, stream);
+}
 cudaError_t launch_cache(const CacheProblem& p, cudaStream_t stream);
 
 // Threads that work on one head row in the cache kernel, and the most a CTA
