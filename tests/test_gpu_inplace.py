@@ -149,7 +149,7 @@ def test_rejected_arguments_raise(rope_gpu):
     x = torch.zeros(1, 2, 2, 64, device="cuda")
     c = torch.ones(1, 2, 1, 64, device="cuda")
     with pytest.raises(R.RopeError) as e:
-        R.rope_inplace_partial(x, c, c, rotary_mode=0)
+        R.rope_inplace_partial(x, c, c, rotary_mode=2)
     assert e.value.status == R.ROPE_ERR_PARAM_INVALID
     with pytest.raises(R.RopeError):
         R.rope_inplace_partial(x, c, c, partial_slice=[0, 32])  # cos width != slice
