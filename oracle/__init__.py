@@ -60,7 +60,7 @@ def _get_lib():
         lib.oracle_rope_with_sin_cos_cache.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
-            ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int]
+            ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
         lib.oracle_rope_with_sin_cos_cache.restype = ctypes.c_int64
         _lib = lib
     return _lib
@@ -136,7 +136,7 @@ def inplace_partial_rotary_mul(x: torch.Tensor, cos: torch.Tensor, sin: torch.Te
 
 def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: torch.Tensor,
                             cache: torch.Tensor, head_size: int, is_neox: bool = True,
-                            mrope_section: Optional[Sequence[int]] = None
+                            mrope_section: Optional[Sequence[int]] = None, cache_mode: int = 0
                             ) -> Tuple[torch.Tensor, torch.Tensor, int]:
     """Oracle of the cache-indexed operator.
 
@@ -156,7 +156,8 @@ def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: t
     T = q.shape[0]
     skipped = _get_lib().oracle_rope_with_sin_cos_cache(
         pos.data_ptr(), sec_ptr, sec_len, q.data_ptr(), q.shape[1], k.data_ptr(), k.shape[1], T,
-        c.data_ptr(), c.shape[0], c.shape[1], _CODE[c.dtype], int(head_size), 1 if is_neox else 0)
+        c.data_ptr(), c.shape[0], c.shape[1], _CODE[c.dtype], int(head_size), 1 if is_neox else 0,
+        int(cache_mode))
     if skipped < 0:
         raise ValueError("oracle rejected the inputs (allocation or mrope section sum)")
     return q, k, int(skipped)

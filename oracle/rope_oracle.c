@@ -39,7 +39,11 @@
  *      cos and the sin index i take row k of the positions.  The 3- and
  *      4-section forms mean the same thing.  mrope is on when the section is
  *      given and its first element is > 0 (the kernel test the page reports).
- *  (6) [RSCC §约束说明 item 5] only says positions should be < maxSeqLen.  A
+ *  (6) [RSCC §V2 接口：cacheMode 扩展] cacheMode 1, three sections: the result
+ *      starts as row 0's cos (sin) and the indices 1, 4, 7, ... and 2, 5, 8, ...
+ *      below 3*mropeSection[1] are replaced from rows 1 and 2.  The page bounds
+ *      both runs by mropeSection[1]; taken literally.
+ *  (7) [RSCC §约束说明 item 5] only says positions should be < maxSeqLen.  A
  *      token with any position outside [0, maxSeqLen) is left untouched and
  *      counted in the return value.
  */
@@ -260,6 +264,8 @@ static void rotate_head(void* buf, int dt, int64_t off, int64_t R, const double*
  * query: [num_tokens, q_cols], key: [num_tokens, k_cols]; q_cols and k_cols are
  *        multiples of head_size.  Both rewritten in place.
  * cache: [max_seq, R]; row = cos (first R/2) then sin (last R/2).
+ * cache_mode (mrope only): 0 splices the sections in order (the V1 rule);
+ * 1 is the V2 interleaved splice of [RSCC §V2 接口：cacheMode 扩展].
  * Returns the number of tokens left untouched for an out-of-range position,
  * or -1 on allocation failure.
  */
@@ -267,7 +273,7 @@ int64_t oracle_rope_with_sin_cos_cache(const int64_t* positions, const int64_t* 
                                        int64_t section_len, void* query, int64_t q_cols, void* key,
                                        int64_t k_cols, int64_t num_tokens, const void* cache,
                                        int64_t max_seq, int64_t R, int dt, int64_t head_size,
-                                       int is_neox) {
+                                       int is_neox, int cache_mode) {
   const int mrope = mrope_section != NULL && section_len > 0 && mrope_section[0] > 0;
   const int64_t rows = mrope ? section_len : 1;
   const int64_t half = R / 2;
@@ -306,6 +312,22 @@ int64_t oracle_rope_with_sin_cos_cache(const int64_t* positions, const int64_t* 
       for (int64_t i = 0; i < half; ++i) {
         cosv[i] = cos_sin[i];
         sinv[i] = cos_sin[half + i];
+      }
+    } else if (cache_mode == 1) {
+      /* V2 interleaved splice: start from row 0, then indices 1, 4, 7, ... below
+       * 3*mropeSection[1] take row 1 and indices 2, 5, 8, ... below the same
+       * bound take row 2 */
+      for (int64_t i = 0; i < half; ++i) {
+        cosv[i] = cos_sin[i];
+        sinv[i] = cos_sin[half + i];
+      }
+      for (int64_t i = 1; i < 3 * mrope_section[1] && i < half; i += 3) {
+        cosv[i] = cos_sin[1 * R + i];
+        sinv[i] = cos_sin[1 * R + half + i];
+      }
+      for (int64_t i = 2; i < 3 * mrope_section[1] && i < half; i += 3) {
+        cosv[i] = cos_sin[2 * R + i];
+        sinv[i] = cos_sin[2 * R + half + i];
       }
     } else {
       int64_t lo = 0;

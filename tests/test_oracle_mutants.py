@@ -38,12 +38,18 @@ MUTANTS = [
     ("GPT-J output concatenated instead of interleaved",
      "out[2 * i] = o1;\n      out[2 * i + 1] = o2;", "out[i] = o1;\n      out[half + i] = o2;"),
     ("cos and sin halves swapped",
-     "cosv[i] = cos_sin[i];\n        sinv[i] = cos_sin[half + i];",
-     "cosv[i] = cos_sin[half + i];\n        sinv[i] = cos_sin[i];"),
+     "if (!mrope) {\n      for (int64_t i = 0; i < half; ++i) {\n        cosv[i] = cos_sin[i];\n        sinv[i] = cos_sin[half + i];",
+     "if (!mrope) {\n      for (int64_t i = 0; i < half; ++i) {\n        cosv[i] = cos_sin[half + i];\n        sinv[i] = cos_sin[i];"),
     ("mrope ignores the section row for cos",
      "cosv[i] = cos_sin[k * R + i];", "cosv[i] = cos_sin[i];"),
     ("mrope sin read from the cos half",
      "sinv[i] = cos_sin[k * R + half + i];", "sinv[i] = cos_sin[k * R + i];"),
+    ("interleaved splice: row 2 bound from the wrong section",
+     "for (int64_t i = 2; i < 3 * mrope_section[1] && i < half; i += 3) {",
+     "for (int64_t i = 2; i < 3 * mrope_section[0] && i < half; i += 3) {"),
+    ("interleaved splice: row 1 stride start off by one",
+     "for (int64_t i = 1; i < 3 * mrope_section[1] && i < half; i += 3) {",
+     "for (int64_t i = 0; i < 3 * mrope_section[1] && i < half; i += 3) {"),
     ("rounding ties away from zero",
      "double m = nearbyint(ldexp(a, (f.p - 1) - E));", "double m = round(ldexp(a, (f.p - 1) - E));"),
     ("rounding by truncation",

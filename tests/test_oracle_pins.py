@@ -583,3 +583,56 @@ def test_backward_noop_and_untouched_columns():
     assert _same_bits(oracle.inplace_partial_rotary_mul(case.x, case.cos, case.sin, 8, 8, backward=True), case.x)
     dx = oracle.inplace_partial_rotary_mul(case.x, case.cos, case.sin, 8, 24, backward=True)
     assert _same_bits(dx[..., :8], case.x[..., :8]) and _same_bits(dx[..., 24:], case.x[..., 24:])
+
+
+# ----------------------------------------------------------------------------
+# cache-indexed operator: V2 interleaved splice (cacheMode 1)
+# ----------------------------------------------------------------------------
+
+def test_interleaved_cache_mode_hand_cases():
+    g = _load("mrope_interleaved_cache_mode_hand_case.json")
+    R = g["rotary_dim"]
+    half = R // 2
+    cache = torch.zeros(5, R)
+    for r in range(5):
+        cache[r, :half] = torch.arange(half) + 100 * r
+    q = torch.ones(1, R)
+    pos = torch.tensor(g["positions"], dtype=torch.int64)
+    for key, spec in g["cases"].items():
+        sec = [int(v) for v in key.split(",")]
+        qo, ko, _ = oracle.rope_with_sin_cos_cache(pos, q, q.clone(), cache, R, True, sec, cache_mode=1)
+        # positions rows hold 1, 2, 3: row k of the splice reads cache row k + 1
+        want = [100 * (r + 1) + i for i, r in enumerate(spec["rows"])] * 2
+        assert qo.reshape(-1).tolist() == want and ko.reshape(-1).tolist() == want, key
+
+
+def test_interleaved_cache_mode_equal_rows_is_rope():
+    c = W.cache_case("t", 27, 31, 2, 2, 128, 128, 600, torch.bfloat16, False)
+    pos3 = c.positions[None, :].expand(3, -1).contiguous()
+    a = oracle.rope_with_sin_cos_cache(c.positions, c.query, c.key, c.cache, 128, False)
+    b = oracle.rope_with_sin_cos_cache(pos3, c.query, c.key, c.cache, 128, False, [24, 20, 20], cache_mode=1)
+    assert _same_bits(a[0], b[0]) and _same_bits(a[1], b[1])
+
+
+@pytest.mark.parametrize("section", [[24, 20, 20], [16, 24, 24], [11, 11, 10]])
+def test_interleaved_cache_mode_matches_complex_form(section):
+    R = 2 * sum(section)
+    c = W.cache_case("t", 28, 23, 2, 1, R, R, 400, torch.float32, True, mrope_section=section)
+    qo, ko, sk = oracle.rope_with_sin_cos_cache(c.positions, c.query, c.key, c.cache, R, True, section,
+                                                cache_mode=1)
+    half = R // 2
+    owner = np.zeros(half, dtype=np.int64)  # row of each cos index, written out from the rule
+    for i in range(half):
+        if i < 3 * section[1] and i % 3 == 1:
+            owner[i] = 1
+        elif i < 3 * section[1] and i % 3 == 2:
+            owner[i] = 2
+    tab = c.cache.double().numpy()
+    rows = c.positions.numpy()[owner, :].T
+    idx = np.arange(half)[None, :]
+    cos, sin = tab[rows, idx], tab[rows, half + idx]
+    for got, x in ((qo, c.query), (ko, c.key)):
+        h = x.double().numpy().reshape(23, -1, R)
+        z = (h[..., :half] + 1j * h[..., half:]) * (cos + 1j * sin)[:, None, :]
+        ref = np.concatenate([z.real, z.imag], axis=-1).reshape(23, -1)
+        assert _ulp_dist(got, oracle.round_to(ref, torch.float32)).max() <= 1
