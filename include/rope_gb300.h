@@ -1,11 +1,13 @@
 /*
  * rope_gb300.h -- C ABI of the GB300 (sm_103a) rotary position embedding library.
  *
- * Two operators, each one asynchronous call on a caller-given CUDA stream:
+ * Two operators, each an asynchronous call on a caller-given CUDA stream:
  *
- *   rope_inplace_partial     in-place partial-slice interleave RoPE on a BSND tensor
- *   rope_with_sin_cos_cache  cos/sin-cache-indexed RoPE of query and key (rope / mrope,
- *                            GPT-NeoX or GPT-J style)
+ *   rope_inplace_partial          in-place partial-slice RoPE on a BSND tensor
+ *                                 (interleave or half mode), and its backward
+ *   rope_with_sin_cos_cache(_v2)  cos/sin-cache-indexed RoPE of query and key (rope /
+ *                                 mrope, GPT-NeoX or GPT-J style; V2: interleaved mrope
+ *                                 splice, strided inputs, separate outputs)
  *
  * Sources (web pages, cited by title and section):
  *  [IPRM] "CANN ops-transformer 的 aclnnInplacePartialRotaryMul 算子：Inplace
@@ -43,7 +45,7 @@
 extern "C" {
 #endif
 
-#define ROPE_ABI_VERSION 2
+#define ROPE_ABI_VERSION 3
 
 typedef enum {
   ROPE_F32 = 0,  /* IEEE binary32 */
@@ -159,6 +161,36 @@ int rope_with_sin_cos_cache(const rope_tensor_t* positions, const rope_tensor_t*
                             const rope_tensor_t* key, const rope_tensor_t* cos_sin_cache,
                             int64_t head_size, int64_t rotary_dim, int32_t is_neox,
                             const int64_t* mrope_section, int64_t mrope_section_len, void* stream);
+
+/*
+ * Cache-indexed RoPE, V2 form: the V1 operation plus the interleaved mrope
+ * splice, strided inputs and separate outputs.
+ * [RSCC §V2 接口：cacheMode 扩展; §算子定义与属性 (qStride/kStride: row strides of
+ *  query/key for non-contiguous inputs); §接口原型 (queryOut/keyOut)]
+ *
+ *   cache_mode        0: the sections are spliced in order, as in V1.
+ *                     1: interleaved splice (three-section mrope only): cos and sin
+ *                     start as the position row 0 values; indices i < 3*mrope_section[1]
+ *                     with i % 3 == 1 take row 1, with i % 3 == 2 take row 2.
+ *   query_row_stride  elements between the starts of consecutive query rows (0: the row
+ *   key_row_stride    width, i.e. contiguous).  At least the row width, and a multiple of
+ *                     16 bytes, so that query/key may be views into a fused QKV buffer.
+ *   query_out,        NULL, NULL: rotate in place (only the first R columns of each head
+ *   key_out           are written).  Otherwise contiguous [numTokens, ...] tensors of the
+ *                     inputs' logical shape and dtype, 16-byte aligned, that receive the
+ *                     whole rows: rotated columns and pass-through columns copied.  An
+ *                     output equal to its input (same pointer, contiguous rows) means in
+ *                     place; any other overlap of outputs with inputs is rejected.  Tokens
+ *                     with an out-of-range position leave their output rows unwritten.
+ *
+ * Every other argument, check and status value is that of rope_with_sin_cos_cache.
+ */
+int rope_with_sin_cos_cache_v2(const rope_tensor_t* positions, const rope_tensor_t* query,
+                               const rope_tensor_t* key, const rope_tensor_t* cos_sin_cache,
+                               int64_t head_size, int64_t rotary_dim, int32_t is_neox,
+                               const int64_t* mrope_section, int64_t mrope_section_len, int32_t cache_mode,
+                               int64_t query_row_stride, int64_t key_row_stride, const rope_tensor_t* query_out,
+                               const rope_tensor_t* key_out, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device-side error word of the

@@ -29,7 +29,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(rope_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(rope_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.rope_abi_version() == 2
+    assert lib.rope_abi_version() == 3
     for st in (C.ROPE_OK, C.ROPE_ERR_PARAM_NULLPTR, C.ROPE_ERR_PARAM_INVALID, C.ROPE_ERR_CUDA, 12345):
         s = C.status_string(st)
         assert isinstance(s, str) and s
@@ -228,3 +228,33 @@ def test_python_binding_refuses_cpu_tensors():
     c = torch.ones(1, 2, 1, 8)
     with pytest.raises(ValueError):
         C.rope_inplace_partial(x, c, c)
+
+
+def _v2(lib, pos, q, k, c, head_size=64, R=None, neox=1, section=None, mode=0, qs=0, ks=0, qo=None, ko=None):
+    R = (c.shape[1] if c is not None else 64) if R is None else R
+    sec, n = None, 0
+    if section is not None:
+        n = len(section)
+        sec = (ctypes.c_int64 * max(1, n))(*section)
+    ref = lambda t: ctypes.byref(t) if t is not None else None  # noqa: E731
+    return lib.rope_with_sin_cos_cache_v2(ref(pos), ref(q), ref(k), ref(c), head_size, R, neox, sec, n, mode,
+                                          qs, ks, ref(qo), ref(ko), None)
+
+
+@pytest.mark.parametrize("case,status", [
+    (dict(mode=2), C.ROPE_ERR_PARAM_INVALID),                                   # unknown cache mode
+    (dict(mode=1), C.ROPE_ERR_PARAM_INVALID),                                   # interleaved splice needs mrope
+    (dict(mode=1, section=[8, 8, 8, 8], pos=_d(C.I64, (4, T))), C.ROPE_ERR_PARAM_INVALID),  # and 3 sections
+    (dict(qs=200), C.ROPE_ERR_PARAM_INVALID),                                   # stride below the row width
+    (dict(qs=260), C.ROPE_ERR_PARAM_INVALID),                                   # stride not a 16-byte multiple
+    (dict(qo=_d(C.BF16, (T, 256), FAKE * 8)), C.ROPE_ERR_PARAM_NULLPTR),        # key_out missing
+    (dict(qo=_d(C.BF16, (T, 128), FAKE * 8), ko=_d(C.BF16, (T, 128), FAKE * 9)), C.ROPE_ERR_PARAM_INVALID),
+    (dict(qo=_d(C.F16, (T, 256), FAKE * 8), ko=_d(C.BF16, (T, 128), FAKE * 9)), C.ROPE_ERR_PARAM_INVALID),
+    (dict(qo=_d(C.BF16, (T, 256), FAKE + 64), ko=_d(C.BF16, (T, 128), FAKE * 9)), C.ROPE_ERR_PARAM_INVALID),
+])
+def test_cache_v2_rejections(lib, case, status):
+    p, q, k, c = good()
+    args = dict(pos=p, q=q, k=k, c=c)
+    args.update(case)
+    pos, q, k, c = args.pop("pos"), args.pop("q"), args.pop("k"), args.pop("c")
+    assert _v2(lib, pos, q, k, c, **args) == status

@@ -26,7 +26,7 @@ ROPE_ERR_CUDA = 561000
 ROPE_DEVICE_POSITION_OUT_OF_RANGE = 1
 
 EXPORTED = ("rope_inplace_partial", "rope_inplace_partial_backward", "rope_with_sin_cos_cache",
-            "rope_get_device_error",
+            "rope_with_sin_cos_cache_v2", "rope_get_device_error",
             "rope_status_string", "rope_launch_count", "rope_abi_version")
 
 
@@ -63,6 +63,10 @@ def load() -> ctypes.CDLL:
     lib.rope_with_sin_cos_cache.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                             ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_void_p]
     lib.rope_with_sin_cos_cache.restype = ctypes.c_int
+    lib.rope_with_sin_cos_cache_v2.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                               ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_int32,
+                                               ctypes.c_int64, ctypes.c_int64, P, P, ctypes.c_void_p]
+    lib.rope_with_sin_cos_cache_v2.restype = ctypes.c_int
     lib.rope_get_device_error.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.rope_get_device_error.restype = ctypes.c_int
     lib.rope_status_string.argtypes = [ctypes.c_int]
@@ -99,6 +103,18 @@ def tensor_desc(t: torch.Tensor) -> RopeTensor:
     if t.dtype not in DTYPE_CODE:
         raise ValueError("unsupported dtype %s" % t.dtype)
     return describe(t.data_ptr(), DTYPE_CODE[t.dtype], tuple(t.shape))
+
+
+def rows_desc(t: torch.Tensor):
+    """Describe a 2-D CUDA tensor whose rows may be strided (unit column
+    stride); returns (descriptor, row stride in elements)."""
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor, got one on %s" % t.device)
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError("expected a 2-D tensor with contiguous rows")
+    if t.dtype not in DTYPE_CODE:
+        raise ValueError("unsupported dtype %s" % t.dtype)
+    return describe(t.data_ptr(), DTYPE_CODE[t.dtype], tuple(t.shape)), int(t.stride(0))
 
 
 def _stream_handle(t: torch.Tensor, stream) -> int:
@@ -157,22 +173,40 @@ def rope_inplace_partial_backward(grad: torch.Tensor, cos: torch.Tensor, sin: to
 def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: torch.Tensor,
                             cos_sin_cache: torch.Tensor, head_size: int, rotary_dim: Optional[int] = None,
                             is_neox: bool = True, mrope_section: Optional[Sequence[int]] = None,
-                            stream=None) -> None:
-    """Cache-indexed RoPE of ``query`` and ``key`` in place (rope or mrope mode)."""
+                            stream=None, *, cache_mode: int = 0, query_out: Optional[torch.Tensor] = None,
+                            key_out: Optional[torch.Tensor] = None) -> None:
+    """Cache-indexed RoPE of ``query`` and ``key`` (rope or mrope mode).
+
+    In place unless ``query_out``/``key_out`` are given.  ``query``/``key`` may
+    be strided row views (e.g. slices of a fused QKV tensor); ``cache_mode=1``
+    selects the interleaved mrope splice.  Contiguous in-place calls with
+    ``cache_mode=0`` use the V1 entry point, everything else the V2 one."""
     lib = load()
     R = int(cos_sin_cache.shape[1]) if rotary_dim is None else int(rotary_dim)
-    dp, dq, dk, dc = (tensor_desc(positions), tensor_desc(query), tensor_desc(key),
-                      tensor_desc(cos_sin_cache))
+    dp, dc = tensor_desc(positions), tensor_desc(cos_sin_cache)
+    dq, qs = rows_desc(query)
+    dk, ks = rows_desc(key)
     sec = None
     n_sec = 0
     if mrope_section is not None:
         n_sec = len(mrope_section)
         sec = (ctypes.c_int64 * max(1, n_sec))(*[int(v) for v in mrope_section])
-    st = lib.rope_with_sin_cos_cache(ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc),
-                                     int(head_size), R, 1 if is_neox else 0, sec, n_sec,
-                                     _stream_handle(query, stream))
+    handle = _stream_handle(query, stream)
+    contiguous = qs == query.shape[1] and ks == key.shape[1]
+    if cache_mode == 0 and query_out is None and key_out is None and contiguous:
+        st = lib.rope_with_sin_cos_cache(ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc),
+                                         int(head_size), R, 1 if is_neox else 0, sec, n_sec, handle)
+        what = "rope_with_sin_cos_cache"
+    else:
+        dqo = tensor_desc(query_out) if query_out is not None else None
+        dko = tensor_desc(key_out) if key_out is not None else None
+        st = lib.rope_with_sin_cos_cache_v2(ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc),
+                                            int(head_size), R, 1 if is_neox else 0, sec, n_sec, int(cache_mode),
+                                            qs, ks, ctypes.byref(dqo) if dqo is not None else None,
+                                            ctypes.byref(dko) if dko is not None else None, handle)
+        what = "rope_with_sin_cos_cache_v2"
     if st != ROPE_OK:
-        raise RopeError(st, "rope_with_sin_cos_cache")
+        raise RopeError(st, what)
 
 
 def get_device_error(stream=None, device=None) -> int:

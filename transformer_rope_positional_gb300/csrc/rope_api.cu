@@ -134,24 +134,11 @@ int inplace_call(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_te
   return cuda_status(rope::launch_inplace(p, static_cast<cudaStream_t>(stream)));
 }
 
-}  // namespace
-
-extern "C" {
-
-int rope_inplace_partial(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_tensor_t* sin,
-                         int64_t rotary_mode, int64_t start, int64_t end, void* stream) {
-  return inplace_call(x, cos, sin, rotary_mode, start, end, false, stream);
-}
-
-int rope_inplace_partial_backward(const rope_tensor_t* grad, const rope_tensor_t* cos, const rope_tensor_t* sin,
-                                  int64_t rotary_mode, int64_t start, int64_t end, void* stream) {
-  return inplace_call(grad, cos, sin, rotary_mode, start, end, true, stream);
-}
-
-int rope_with_sin_cos_cache(const rope_tensor_t* positions, const rope_tensor_t* query,
-                            const rope_tensor_t* key, const rope_tensor_t* cos_sin_cache,
-                            int64_t head_size, int64_t rotary_dim, int32_t is_neox,
-                            const int64_t* mrope_section, int64_t mrope_section_len, void* stream) {
+// Checks shared by the V1 and V2 cache calls, then the launch.
+int cache_call(const rope_tensor_t* positions, const rope_tensor_t* query, const rope_tensor_t* key,
+               const rope_tensor_t* cos_sin_cache, int64_t head_size, int64_t rotary_dim, int32_t is_neox,
+               const int64_t* mrope_section, int64_t mrope_section_len, int32_t cache_mode, int64_t q_row_stride,
+               int64_t k_row_stride, const rope_tensor_t* query_out, const rope_tensor_t* key_out, void* stream) {
   if (!positions || !query || !key || !cos_sin_cache) return ROPE_ERR_PARAM_NULLPTR;
   // dtypes: positions int64; query, key and cache the same floating type
   if (positions->dtype != kI64 || !is_float(query->dtype)) return ROPE_ERR_PARAM_INVALID;
@@ -188,10 +175,43 @@ int rope_with_sin_cos_cache(const rope_tensor_t* positions, const rope_tensor_t*
   } else {
     if (positions->ndim != 1 || positions->shape[0] != T) return ROPE_ERR_PARAM_INVALID;
   }
+  // V2: interleaved splice only for three-section mrope
+  if (cache_mode != 0 && cache_mode != 1) return ROPE_ERR_PARAM_INVALID;
+  if (cache_mode == 1 && !(mrope && mrope_section_len == 3)) return ROPE_ERR_PARAM_INVALID;
+  // row strides (elements): 0 means contiguous rows
+  const int64_t qw = query->shape[1], kw = key->shape[1];
+  const int64_t qs = q_row_stride ? q_row_stride : qw, ks = k_row_stride ? k_row_stride : kw;
+  const int64_t esz = query->dtype == kF32 ? 4 : 2;
+  if (qs < qw || ks < kw || (qs * esz) % 16 || (ks * esz) % 16) return ROPE_ERR_PARAM_INVALID;
+  // outputs: both or neither; contiguous, same shape and dtype as the inputs
+  if ((query_out == nullptr) != (key_out == nullptr)) return ROPE_ERR_PARAM_NULLPTR;
+  if (query_out) {
+    if (query_out->dtype != query->dtype || key_out->dtype != key->dtype) return ROPE_ERR_PARAM_INVALID;
+    if (query_out->ndim != 2 || key_out->ndim != 2 || query_out->shape[0] != T || query_out->shape[1] != qw ||
+        key_out->shape[0] != T || key_out->shape[1] != kw)
+      return ROPE_ERR_PARAM_INVALID;
+    if (!query_out->data || !key_out->data) return ROPE_ERR_PARAM_NULLPTR;
+    if (!aligned(query_out->data, 16) || !aligned(key_out->data, 16)) return ROPE_ERR_PARAM_INVALID;
+  }
   if (!positions->data || !query->data || !key->data || !cos_sin_cache->data) return ROPE_ERR_PARAM_NULLPTR;
   if (!aligned(positions->data, 8) || !aligned(query->data, 16) || !aligned(key->data, 16) ||
       !aligned(cos_sin_cache->data, 16))
     return ROPE_ERR_PARAM_INVALID;
+  // an output that is its input (same pointer, contiguous rows) means in place;
+  // any other overlap between the outputs and the inputs is rejected
+  bool in_place = query_out == nullptr;
+  if (!in_place && query_out->data == query->data && key_out->data == key->data && qs == qw && ks == kw)
+    in_place = true;
+  if (!in_place) {
+    const char* spans[4][2] = {
+        {static_cast<const char*>(query->data), static_cast<const char*>(query->data) + ((T - 1) * qs + qw) * esz},
+        {static_cast<const char*>(key->data), static_cast<const char*>(key->data) + ((T - 1) * ks + kw) * esz},
+        {static_cast<const char*>(query_out->data), static_cast<const char*>(query_out->data) + T * qw * esz},
+        {static_cast<const char*>(key_out->data), static_cast<const char*>(key_out->data) + T * kw * esz}};
+    for (int o = 2; o < 4; ++o)
+      for (int i = 0; i < 4; ++i)
+        if (i != o && spans[o][0] < spans[i][1] && spans[i][0] < spans[o][1]) return ROPE_ERR_PARAM_INVALID;
+  }
 
   rope::CacheProblem p;
   p.positions = static_cast<const int64_t*>(positions->data);
@@ -208,10 +228,47 @@ int rope_with_sin_cos_cache(const rope_tensor_t* positions, const rope_tensor_t*
   p.is_neox = is_neox != 0;
   p.mrope_rows = mrope ? (int32_t)mrope_section_len : 0;
   for (int i = 0; i < 4; ++i) p.section_end[i] = section_end[i];
+  p.cache_mode = cache_mode;
+  p.q_stride = qs;
+  p.k_stride = ks;
+  p.query_out = in_place ? nullptr : query_out->data;
+  p.key_out = in_place ? nullptr : key_out->data;
   // one team of threads must fit one block of the cache kernel
   if (rope::cache_team_threads(p) > rope::cache_max_team_threads()) return ROPE_ERR_PARAM_INVALID;
   if (p.hq + p.hk > (int64_t)1 << 30 || head_size > (int64_t)1 << 30) return ROPE_ERR_PARAM_INVALID;
   return cuda_status(rope::launch_cache(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int rope_inplace_partial(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_tensor_t* sin,
+                         int64_t rotary_mode, int64_t start, int64_t end, void* stream) {
+  return inplace_call(x, cos, sin, rotary_mode, start, end, false, stream);
+}
+
+int rope_inplace_partial_backward(const rope_tensor_t* grad, const rope_tensor_t* cos, const rope_tensor_t* sin,
+                                  int64_t rotary_mode, int64_t start, int64_t end, void* stream) {
+  return inplace_call(grad, cos, sin, rotary_mode, start, end, true, stream);
+}
+
+int rope_with_sin_cos_cache(const rope_tensor_t* positions, const rope_tensor_t* query,
+                            const rope_tensor_t* key, const rope_tensor_t* cos_sin_cache,
+                            int64_t head_size, int64_t rotary_dim, int32_t is_neox,
+                            const int64_t* mrope_section, int64_t mrope_section_len, void* stream) {
+  return cache_call(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_neox, mrope_section,
+                    mrope_section_len, 0, 0, 0, nullptr, nullptr, stream);
+}
+
+int rope_with_sin_cos_cache_v2(const rope_tensor_t* positions, const rope_tensor_t* query,
+                               const rope_tensor_t* key, const rope_tensor_t* cos_sin_cache,
+                               int64_t head_size, int64_t rotary_dim, int32_t is_neox,
+                               const int64_t* mrope_section, int64_t mrope_section_len, int32_t cache_mode,
+                               int64_t query_row_stride, int64_t key_row_stride, const rope_tensor_t* query_out,
+                               const rope_tensor_t* key_out, void* stream) {
+  return cache_call(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_neox, mrope_section,
+                    mrope_section_len, cache_mode, query_row_stride, key_row_stride, query_out, key_out, stream);
 }
 
 int rope_get_device_error(void* stream, int32_t* code) {

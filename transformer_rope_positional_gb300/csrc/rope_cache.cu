@@ -51,6 +51,7 @@ constexpr unsigned kPositionOutOfRange = 1u;
 struct CacheArgs {
   int64_t T;
   int64_t max_seq;
+  int64_t q_stride, k_stride;  // elements between consecutive input rows
   int64_t items;       // T * head_chunks
   int32_t head_chunks;  // ceil((hq + hk) / U): chunks of U consecutive heads per token
   int32_t hq, hk;
@@ -59,6 +60,8 @@ struct CacheArgs {
   int32_t chunks;  // threads per row (C)
   int32_t mrope_rows;
   int32_t section_end[4];
+  int32_t cache_mode;      // 0 sectioned splice, 1 interleaved splice (V2)
+  int32_t interleave_end;  // cache_mode 1: indices below 3 * mropeSection[1] interleave
 };
 
 // Section holding cos index i.  section_end[] holds cumulative ends and the
@@ -95,6 +98,24 @@ __device__ __forceinline__ bool gather_cos_sin(const int64_t* __restrict__ pos, 
   if (p0 < 0 || p0 >= a.max_seq || p1 < 0 || p1 >= a.max_seq || p2 < 0 || p2 >= a.max_seq || p3 < 0 ||
       p3 >= a.max_seq)
     return false;
+  if (a.cache_mode == 1) {
+    // V2 interleaved splice: row 0, except indices below interleave_end whose
+    // remainder mod 3 is 1 (row 1) or 2 (row 2)
+    if (i0 >= a.interleave_end) {
+      const T* rowp = cache + p0 * a.R;
+      load_f32<T, NC>(cf, rowp + i0);
+      load_f32<T, NC>(sf, rowp + half + i0);
+    } else {
+#pragma unroll
+      for (int e = 0; e < NC; ++e) {
+        const int i = i0 + e;
+        const T* rowp = cache + select_row(i < a.interleave_end ? i % 3 : 0, p0, p1, p2, p3) * a.R;
+        cf[e] = widen(__ldg(rowp + i));
+        sf[e] = widen(__ldg(rowp + half + i));
+      }
+    }
+    return true;
+  }
   const int k0 = section_of(i0, a);
   const int k1 = section_of(i0 + NC - 1, a);
   if (k0 == k1) {  // the whole chunk sits in one section: one vector per half
@@ -112,10 +133,12 @@ __device__ __forceinline__ bool gather_cos_sin(const int64_t* __restrict__ pos, 
   return true;
 }
 
-template <typename T, bool NEOX, int VEC>
+// OUT: results go to the contiguous outputs qo/ko (pass-through columns
+// copied there); otherwise query/key are rewritten in place.
+template <typename T, bool NEOX, bool OUT, int VEC>
 __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
     cache_kernel(const int64_t* __restrict__ pos, T* __restrict__ q, T* __restrict__ k,
-                 const T* __restrict__ cache, CacheArgs a) {
+                 const T* __restrict__ cache, T* __restrict__ qo, T* __restrict__ ko, CacheArgs a) {
   constexpr int U = kRowsInFlight;
   constexpr int NC = NEOX ? VEC : VEC / 2;  // cos (and sin) indices owned per thread
   const int C = a.chunks;
@@ -139,8 +162,8 @@ __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int h = h0 + (u < n ? u : 0);
-      base[u] = h < a.hq ? q + (t * a.hq + h) * (int64_t)a.head_size
-                         : k + (t * a.hk + (h - a.hq)) * (int64_t)a.head_size;
+      base[u] = h < a.hq ? q + t * a.q_stride + h * (int64_t)a.head_size
+                         : k + t * a.k_stride + (h - a.hq) * (int64_t)a.head_size;
       if (u < n) {
         if constexpr (NEOX) {
           load_vec<true>(x1[u], base[u] + i0);
@@ -161,6 +184,12 @@ __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (u >= n) break;
+      T* dst = base[u];
+      if constexpr (OUT) {
+        const int h = h0 + u;
+        dst = h < a.hq ? qo + (t * a.hq + h) * (int64_t)a.head_size
+                       : ko + (t * a.hk + (h - a.hq)) * (int64_t)a.head_size;
+      }
       if constexpr (NEOX) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
@@ -169,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
           x1[u].e[e] = narrow<T>(diff_of_products(a1, cf[e], a2, sf[e]));
           x2[u].e[e] = narrow<T>(diff_of_products(a2, cf[e], -a1, sf[e]));
         }
-        store_vec(base[u] + i0, x1[u]);
-        store_vec(base[u] + half + i0, x2[u]);
+        store_vec(dst + i0, x1[u]);
+        store_vec(dst + half + i0, x2[u]);
       } else {
 #pragma unroll
         for (int e = 0; e < NC; ++e) {
@@ -179,18 +208,28 @@ __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
           x1[u].e[2 * e] = narrow<T>(diff_of_products(a1, cf[e], a2, sf[e]));
           x1[u].e[2 * e + 1] = narrow<T>(diff_of_products(a2, cf[e], -a1, sf[e]));
         }
-        store_vec(base[u] + 2 * i0, x1[u]);
+        store_vec(dst + 2 * i0, x1[u]);
+      }
+      if constexpr (OUT) {
+        // pass-through columns [R, head_size) are copied to the output row
+        for (int j = a.R + c * VEC; j < a.head_size; j += C * VEC) {
+          Vec<T, VEC> v;
+          load_vec<true>(v, base[u] + j);
+          store_vec(dst + j, v);
+        }
       }
     }
   }
 }
 
-template <typename T, bool NEOX>
+template <typename T, bool NEOX, bool OUT>
 cudaError_t launch_typed(const CacheProblem& p, cudaStream_t stream) {
   constexpr int VEC = 16 / sizeof(T);
   CacheArgs a;
   a.T = p.T;
   a.max_seq = p.max_seq;
+  a.q_stride = p.q_stride;
+  a.k_stride = p.k_stride;
   a.hq = (int32_t)p.hq;
   a.hk = (int32_t)p.hk;
   a.head_size = (int32_t)p.head_size;
@@ -199,22 +238,27 @@ cudaError_t launch_typed(const CacheProblem& p, cudaStream_t stream) {
   a.mrope_rows = p.mrope_rows;
   // ends past the used sections are R/2, so section_of() never counts them
   for (int i = 0; i < 4; ++i) a.section_end[i] = i < p.mrope_rows ? p.section_end[i] : (int32_t)(p.rotary_dim / 2);
+  a.cache_mode = p.cache_mode;
+  a.interleave_end = p.cache_mode == 1 ? 3 * (p.section_end[1] - p.section_end[0]) : 0;
   a.head_chunks = (int32_t)((p.hq + p.hk + kRowsInFlight - 1) / kRowsInFlight);
   a.items = p.T * a.head_chunks;
   const int threads = kThreads;
   const int64_t groups = threads / a.chunks;
   // Persistent grid: the CTAs that fit on the GPU at once stride over the items,
   // P consecutive items per CTA per step.
-  const void* kfn = reinterpret_cast<const void*>(cache_kernel<T, NEOX, VEC>);
-  const int64_t resident = (int64_t)sm_count() * resident_blocks(kfn, threads);
+  auto kernel = cache_kernel<T, NEOX, OUT, VEC>;
+  const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), threads);
   const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
-  return launch_overlapped(cache_kernel<T, NEOX, VEC>, (unsigned)grid, threads, stream, p.positions,
-                           static_cast<T*>(p.query), static_cast<T*>(p.key), static_cast<const T*>(p.cache), a);
+  return launch_overlapped(kernel, (unsigned)grid, threads, stream, p.positions, static_cast<T*>(p.query),
+                           static_cast<T*>(p.key), static_cast<const T*>(p.cache), static_cast<T*>(p.query_out),
+                           static_cast<T*>(p.key_out), a);
 }
 
 template <typename T>
 cudaError_t launch_style(const CacheProblem& p, cudaStream_t stream) {
-  return p.is_neox ? launch_typed<T, true>(p, stream) : launch_typed<T, false>(p, stream);
+  const bool out = p.query_out != nullptr;
+  if (p.is_neox) return out ? launch_typed<T, true, true>(p, stream) : launch_typed<T, true, false>(p, stream);
+  return out ? launch_typed<T, false, true>(p, stream) : launch_typed<T, false, false>(p, stream);
 }
 
 }  // namespace

@@ -39,6 +39,11 @@ struct CacheProblem {
   bool is_neox;
   int32_t mrope_rows;      // 0: rope; 3 or 4: mrope
   int32_t section_end[4];  // cumulative ends of the mrope sections (cos indices)
+  int32_t cache_mode;      // 0: sections spliced in order; 1: interleaved splice
+  int64_t q_stride;        // elements between consecutive query rows
+  int64_t k_stride;        // elements between consecutive key rows
+  void* query_out;         // contiguous outputs, or both NULL for in place
+  void* key_out;
 };
 
 cudaError_t launch_inplace_forward(const InplaceProblem& p, cudaStream_t stream);
