@@ -143,7 +143,8 @@ int rope_inplace_partial_backward(const rope_tensor_t* grad, const rope_tensor_t
  *   cos_sin_cache  2-D [maxSeqLen, R], same dtype as query, 16-byte aligned.
  *   head_size      a multiple of 32 (F16/BF16) or 16 (F32), dividing both row widths.
  *   rotary_dim     R; must equal cos_sin_cache.shape[1]; R <= head_size and a multiple of
- *                  32 (F16/BF16) or 16 (F32).
+ *                  32 (F16/BF16) or 16 (F32); at most 2048 (F16/BF16 NeoX), 1024 (F16/BF16
+ *                  GPT-J, F32 NeoX) or 512 (F32 GPT-J).
  *   is_neox        nonzero: GPT-NeoX rotate_half; zero: GPT-J rotate_interleaved.
  *   mrope_section  HOST pointer to mrope_section_len int64 values, or NULL for rope mode.
  *                  mrope is on when the pointer is non-NULL and mrope_section[0] > 0;

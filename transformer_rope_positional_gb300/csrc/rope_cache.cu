@@ -42,7 +42,7 @@ namespace {
 #define ROPE_CACHE_MIN_BLOCKS 1
 #endif
 #ifndef ROPE_CACHE_THREADS
-#define ROPE_CACHE_THREADS 256
+#define ROPE_CACHE_THREADS 128
 #endif
 constexpr int kRowsInFlight = ROPE_CACHE_ROWS_IN_FLIGHT;  // U: rows loaded before compute, per thread
 constexpr int kThreads = ROPE_CACHE_THREADS;
@@ -78,12 +78,16 @@ __device__ __forceinline__ int64_t select_row(int k, int64_t p0, int64_t p1, int
 // Steps 1-2 for one token: gather cosSin = cache[positions[t]] and split it
 // into this thread's NC cos and NC sin values (first owned index i0).
 // Returns false (nothing loaded) when a position is outside [0, maxSeqLen).
-template <typename T, int NC>
+// How the cos/sin chunk is assembled: plain rope, mrope with the sections
+// spliced in order, mrope with the V2 interleaved splice.
+enum Splice : int { kRope = 0, kSectioned = 1, kInterleaved = 2 };
+
+template <typename T, int NC, int SPLICE>
 __device__ __forceinline__ bool gather_cos_sin(const int64_t* __restrict__ pos, const T* __restrict__ cache,
                                                const CacheArgs& a, int64_t t, int i0, float (&cf)[NC],
                                                float (&sf)[NC]) {
   const int half = a.R / 2;
-  if (a.mrope_rows == 0) {
+  if constexpr (SPLICE == kRope) {
     const int64_t p = __ldg(pos + t);
     if (p < 0 || p >= a.max_seq) return false;
     const T* rowp = cache + p * a.R;
@@ -98,7 +102,7 @@ __device__ __forceinline__ bool gather_cos_sin(const int64_t* __restrict__ pos, 
   if (p0 < 0 || p0 >= a.max_seq || p1 < 0 || p1 >= a.max_seq || p2 < 0 || p2 >= a.max_seq || p3 < 0 ||
       p3 >= a.max_seq)
     return false;
-  if (a.cache_mode == 1) {
+  if constexpr (SPLICE == kInterleaved) {
     // V2 interleaved splice: row 0, except indices below interleave_end whose
     // remainder mod 3 is 1 (row 1) or 2 (row 2)
     if (i0 >= a.interleave_end) {
@@ -135,7 +139,7 @@ __device__ __forceinline__ bool gather_cos_sin(const int64_t* __restrict__ pos, 
 
 // OUT: results go to the contiguous outputs qo/ko (pass-through columns
 // copied there); otherwise query/key are rewritten in place.
-template <typename T, bool NEOX, bool OUT, int VEC>
+template <typename T, bool NEOX, bool OUT, int SPLICE, int VEC>
 __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
     cache_kernel(const int64_t* __restrict__ pos, T* __restrict__ q, T* __restrict__ k,
                  const T* __restrict__ cache, T* __restrict__ qo, T* __restrict__ ko, CacheArgs a) {
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
     }
     // ---- steps 1-2: the token's cos/sin chunk
     float cf[NC], sf[NC];
-    if (!gather_cos_sin<T, NC>(pos, cache, a, t, i0, cf, sf)) {
+    if (!gather_cos_sin<T, NC, SPLICE>(pos, cache, a, t, i0, cf, sf)) {
       // reported once per token, by thread 0 of the group holding head 0
       if (c == 0 && h0 == 0) atomicOr(&g_device_error, kPositionOutOfRange);
       continue;  // leave the token untouched
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
   }
 }
 
-template <typename T, bool NEOX, bool OUT>
+template <typename T, bool NEOX, bool OUT, int SPLICE>
 cudaError_t launch_typed(const CacheProblem& p, cudaStream_t stream) {
   constexpr int VEC = 16 / sizeof(T);
   CacheArgs a;
@@ -246,7 +250,7 @@ cudaError_t launch_typed(const CacheProblem& p, cudaStream_t stream) {
   const int64_t groups = threads / a.chunks;
   // Persistent grid: the CTAs that fit on the GPU at once stride over the items,
   // P consecutive items per CTA per step.
-  auto kernel = cache_kernel<T, NEOX, OUT, VEC>;
+  auto kernel = cache_kernel<T, NEOX, OUT, SPLICE, VEC>;
   const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), threads);
   const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
   return launch_overlapped(kernel, (unsigned)grid, threads, stream, p.positions, static_cast<T*>(p.query),
@@ -254,11 +258,18 @@ cudaError_t launch_typed(const CacheProblem& p, cudaStream_t stream) {
                            static_cast<T*>(p.key_out), a);
 }
 
+template <typename T, bool NEOX, bool OUT>
+cudaError_t launch_splice(const CacheProblem& p, cudaStream_t stream) {
+  if (p.mrope_rows == 0) return launch_typed<T, NEOX, OUT, kRope>(p, stream);
+  if (p.cache_mode == 1) return launch_typed<T, NEOX, OUT, kInterleaved>(p, stream);
+  return launch_typed<T, NEOX, OUT, kSectioned>(p, stream);
+}
+
 template <typename T>
 cudaError_t launch_style(const CacheProblem& p, cudaStream_t stream) {
   const bool out = p.query_out != nullptr;
-  if (p.is_neox) return out ? launch_typed<T, true, true>(p, stream) : launch_typed<T, true, false>(p, stream);
-  return out ? launch_typed<T, false, true>(p, stream) : launch_typed<T, false, false>(p, stream);
+  if (p.is_neox) return out ? launch_splice<T, true, true>(p, stream) : launch_splice<T, true, false>(p, stream);
+  return out ? launch_splice<T, false, true>(p, stream) : launch_splice<T, false, false>(p, stream);
 }
 
 }  // namespace

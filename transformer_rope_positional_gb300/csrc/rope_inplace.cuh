@@ -44,7 +44,7 @@ namespace inplace {
 #define ROPE_INPLACE_ROWS_IN_FLIGHT 4
 #endif
 #ifndef ROPE_INPLACE_THREADS
-#define ROPE_INPLACE_THREADS 256
+#define ROPE_INPLACE_THREADS 128
 #endif
 #ifndef ROPE_INPLACE_MIN_BLOCKS
 #define ROPE_INPLACE_MIN_BLOCKS 1
