@@ -344,35 +344,57 @@ def run_ours(args):
 
 
 def time_next_rows(cases, dev_tensors, calls, steps):
-    """Per-launch time of the in-place operator's backward (interleave) and of
-    its half mode on the [4,4096,32,128] workload.  Sequence per step:
-    backward, NeoX cache launch (flushes L2), half mode, mrope launch."""
+    """Per-launch time of the rows beyond the hot path on the hot path's own
+    workloads: the in-place operator's backward and half mode, the V2 cache
+    operator with the interleaved mrope splice, with separate outputs, and on
+    strided views of a fused QKV buffer.  Each timed launch is followed by a
+    large cache-op launch on other buffers, so every timed launch starts cold."""
     import transformer_rope_positional_gb300 as R
-    c = cases[0]
+    inplace, neox, gptj, mrope = cases
     x, cs, sn = dev_tensors[0]
-    extra = [("inplace_backward_interleave_" + c.name.split("_", 1)[1],
-              R.prepare_inplace_partial(x, cs, sn, 1, [c.start, c.end], backward=True)),
-             ("inplace_half_forward_" + c.name.split("_", 1)[1],
-              R.prepare_inplace_partial(x, cs, sn, 0, [c.start, c.end]))]
-    flushers = [calls[1], calls[3]]
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    p3, q3, k3, c3 = dev_tensors[1]
+    p4, q4, k4, c4 = dev_tensors[2]
+    p5, q5, k5, c5 = dev_tensors[3]
+    tag = inplace.name.split("_", 1)[1]
+    rows = [("inplace_backward_interleave_" + tag, algorithmic_bytes(inplace),
+             R.prepare_inplace_partial(x, cs, sn, 1, [inplace.start, inplace.end], backward=True), calls[1]),
+            ("inplace_half_forward_" + tag, algorithmic_bytes(inplace),
+             R.prepare_inplace_partial(x, cs, sn, 0, [inplace.start, inplace.end]), calls[3])]
+    # V2 interleaved splice on the mrope workload
+    rows.append(("mrope_interleaved_splice_" + mrope.name.split("_", 1)[1], algorithmic_bytes(mrope),
+                 R.prepare_with_sin_cos_cache(p5, q5, k5, c5, mrope.head_size, mrope.rotary_dim, True,
+                                              mrope.mrope_section, cache_mode=1), calls[1]))
+    # V2 separate outputs on the NeoX workload (R == head size: no pass-through)
+    qo, ko = torch.empty_like(q3), torch.empty_like(k3)
+    rows.append(("rope_neox_out_of_place_" + neox.name.split("_", 2)[2], algorithmic_bytes(neox),
+                 R.prepare_with_sin_cos_cache(p3, q3, k3, c3, neox.head_size, neox.rotary_dim, True,
+                                              query_out=qo, key_out=ko), calls[3]))
+    # V2 strided rows: GPT-J workload on q/k views of a fused [T, (16+16+16)*256] QKV buffer
+    T, hs = gptj.tokens, gptj.head_size
+    wq, wk = q4.shape[1], k4.shape[1]
+    qkv = torch.empty(T, wq + wk + wk, dtype=q4.dtype, device=q4.device)
+    qkv[:, :wq].copy_(q4)
+    qkv[:, wq:wq + wk].copy_(k4)
+    rows.append(("rope_gptj_fused_qkv_views_" + gptj.name.split("_", 2)[2], algorithmic_bytes(gptj),
+                 R.prepare_with_sin_cos_cache(p4, qkv[:, :wq], qkv[:, wq:wq + wk], c4, hs, gptj.rotary_dim, False),
+                 calls[1]))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(rows))] for _ in range(steps)]
     for _ in range(3):
-        for (_, call), fl in zip(extra, flushers):
+        for _, _, call, flush in rows:
             call()
-            fl()
+            flush()
     torch.cuda.synchronize()
     torch.cuda._sleep(int(4e6))
     for s_ in range(steps):
-        for i, ((_, call), fl) in enumerate(zip(extra, flushers)):
+        for i, (_, _, call, flush) in enumerate(rows):
             ev[s_][2 * i].record()
             call()
             ev[s_][2 * i + 1].record()
-            fl()
+            flush()
     torch.cuda.synchronize()
     peak, _ = measured_peak()
-    b = algorithmic_bytes(c)
     out = []
-    for i, (name, _) in enumerate(extra):
+    for i, (name, b, _, _) in enumerate(rows):
         ms = [ev[s_][2 * i].elapsed_time(ev[s_][2 * i + 1]) for s_ in range(steps)]
         avg = sum(ms) / len(ms)
         out.append({"workload": name, "bytes_per_launch": b, "launches": steps, "avg_us": round(avg * 1e3, 3),

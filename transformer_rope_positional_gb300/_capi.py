@@ -261,17 +261,32 @@ def prepare_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tenso
 def prepare_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: torch.Tensor,
                                cos_sin_cache: torch.Tensor, head_size: int, rotary_dim: Optional[int] = None,
                                is_neox: bool = True, mrope_section: Optional[Sequence[int]] = None,
-                               stream=None) -> PreparedCall:
+                               stream=None, *, cache_mode: int = 0, query_out: Optional[torch.Tensor] = None,
+                               key_out: Optional[torch.Tensor] = None) -> PreparedCall:
+    """Marshal one cache-operator call once (V1 entry point when the call is a
+    contiguous in-place one with cache_mode 0, else V2)."""
     lib = load()
     R = int(cos_sin_cache.shape[1]) if rotary_dim is None else int(rotary_dim)
-    dp, dq, dk, dc = (tensor_desc(positions), tensor_desc(query), tensor_desc(key),
-                      tensor_desc(cos_sin_cache))
+    dp, dc = tensor_desc(positions), tensor_desc(cos_sin_cache)
+    dq, qs = rows_desc(query)
+    dk, ks = rows_desc(key)
     sec = None
     n_sec = 0
     if mrope_section is not None:
         n_sec = len(mrope_section)
         sec = (ctypes.c_int64 * max(1, n_sec))(*[int(v) for v in mrope_section])
+    handle = _stream_handle(query, stream)
+    contiguous = qs == query.shape[1] and ks == key.shape[1]
+    if cache_mode == 0 and query_out is None and key_out is None and contiguous:
+        args = (ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc), int(head_size), R,
+                1 if is_neox else 0, sec, n_sec, handle)
+        return PreparedCall(lib.rope_with_sin_cos_cache, args,
+                            (positions, query, key, cos_sin_cache, dp, dq, dk, dc, sec), "rope_with_sin_cos_cache")
+    dqo = tensor_desc(query_out) if query_out is not None else None
+    dko = tensor_desc(key_out) if key_out is not None else None
     args = (ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc), int(head_size), R,
-            1 if is_neox else 0, sec, n_sec, _stream_handle(query, stream))
-    return PreparedCall(lib.rope_with_sin_cos_cache, args,
-                        (positions, query, key, cos_sin_cache, dp, dq, dk, dc, sec), "rope_with_sin_cos_cache")
+            1 if is_neox else 0, sec, n_sec, int(cache_mode), qs, ks,
+            ctypes.byref(dqo) if dqo is not None else None, ctypes.byref(dko) if dko is not None else None, handle)
+    return PreparedCall(lib.rope_with_sin_cos_cache_v2, args,
+                        (positions, query, key, cos_sin_cache, query_out, key_out, dp, dq, dk, dc, dqo, dko, sec),
+                        "rope_with_sin_cos_cache_v2")
