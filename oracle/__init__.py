@@ -62,6 +62,12 @@ def _get_lib():
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
         lib.oracle_rope_with_sin_cos_cache.restype = ctypes.c_int64
+        lib.oracle_qkv_rmsnorm_rope_cache.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_qkv_rmsnorm_rope_cache.restype = ctypes.c_int64
         _lib = lib
     return _lib
 
@@ -161,6 +167,31 @@ def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: t
     if skipped < 0:
         raise ValueError("oracle rejected the inputs (allocation or mrope section sum)")
     return q, k, int(skipped)
+
+
+def qkv_rmsnorm_rope_cache(qkv: torch.Tensor, num_q_heads: int, num_k_heads: int, num_v_heads: int,
+                           q_gamma: torch.Tensor, k_gamma: torch.Tensor, eps: float, cache: torch.Tensor,
+                           seq_lens: torch.Tensor, query_start_loc: torch.Tensor, slot_mapping: torch.Tensor,
+                           q_out: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor):
+    """Oracle of the fused QKV split + RMSNorm + RoPE + paged cache write.
+
+    ``q_out``, ``k_cache`` and ``v_cache`` give the initial contents (entries the
+    operator does not write keep them).  Returns ``(q_out, k_cache, v_cache,
+    bad_positions, bad_slots)`` as new CPU tensors."""
+    x = _cpu(qkv)
+    qo, kc, vc = _cpu(q_out).clone(), _cpu(k_cache).clone(), _cpu(v_cache).clone()
+    qg, kg, c = _cpu(q_gamma), _cpu(k_gamma), _cpu(cache)
+    sl, qs, sm = (_cpu(t).to(torch.int64) for t in (seq_lens, query_start_loc, slot_mapping))
+    assert x.dtype == qg.dtype == kg.dtype == c.dtype == qo.dtype == kc.dtype == vc.dtype
+    T = x.shape[0]
+    D = x.shape[1] // (num_q_heads + num_k_heads + num_v_heads)
+    r = _get_lib().oracle_qkv_rmsnorm_rope_cache(
+        x.data_ptr(), _CODE[x.dtype], T, num_q_heads, num_k_heads, num_v_heads, D, qg.data_ptr(), kg.data_ptr(),
+        float(eps), c.data_ptr(), c.shape[0], sl.data_ptr(), qs.data_ptr(), sl.shape[0], sm.data_ptr(),
+        kc.shape[2], kc.shape[0], qo.data_ptr(), kc.data_ptr(), vc.data_ptr())
+    if r < 0:
+        raise MemoryError("oracle allocation failed")
+    return qo, kc, vc, int(r & 0xFFFFFFFF), int(r >> 32)
 
 
 def exact_values(t: torch.Tensor) -> np.ndarray:

@@ -348,3 +348,90 @@ int64_t oracle_rope_with_sin_cos_cache(const int64_t* positions, const int64_t* 
   free(cos_sin); free(cosv); free(sinv); free(xr); free(out);
   return skipped;
 }
+
+/*
+ * Fused QKV split + RMSNorm + RoPE + paged KV-cache write, in the order the
+ * page gives it ["aclnnQkvRmsNormRopeCacheWithKScale" page, section 计算公式],
+ * without its FP8 quantisation and its optional rotation matmul.
+ *
+ * Readings of the page, whose tables are garbled:
+ *  - qkv is [T, (Nq + Nk + Nv) * D], split by heads of D elements;
+ *  - RMSNorm is per head over its D elements, y = x / sqrt(mean(x^2) + eps) * gamma,
+ *    with one gamma of length D per branch (q_gamma, k_gamma);
+ *  - the position of token i of batch b is seqLens[b] - (qsl[b+1] - qsl[b]) + i,
+ *    and cos/sin are the halves of cache row `position` of a [maxSeq, D] cos||sin
+ *    table (the RopeWithSinCosCache convention);
+ *  - RoPE is the page's concat(low*cos - high*sin, high*cos + low*sin) over the
+ *    whole head; V gets neither norm nor RoPE;
+ *  - q_out is [T, Nq * D]; K and V go to caches [numBlocks, N, BlockSize, D] at
+ *    block slot/BlockSize, offset slot%BlockSize; a negative slot means "do not
+ *    cache this token" (padding); everything is stored in the input type.
+ * Tokens whose position falls outside the table leave q_out unwritten and
+ * write no cache; slots at or past numBlocks*BlockSize are not written.
+ * Returns (tokens with a bad position) + 2^32 * (tokens with a bad slot), or
+ * -1 on allocation failure.
+ */
+int64_t oracle_qkv_rmsnorm_rope_cache(const void* qkv, int dt, int64_t T, int64_t nq, int64_t nk, int64_t nv,
+                                      int64_t D, const void* q_gamma, const void* k_gamma, double eps,
+                                      const void* cache, int64_t max_seq, const int64_t* seq_lens,
+                                      const int64_t* qsl, int64_t B, const int64_t* slot_mapping,
+                                      int64_t block_size, int64_t num_blocks, void* q_out, void* k_cache,
+                                      void* v_cache) {
+  const int64_t W = (nq + nk + nv) * D, half = D / 2;
+  double* x = (double*)malloc(sizeof(double) * (size_t)D);
+  double* y = (double*)malloc(sizeof(double) * (size_t)D);
+  double* o = (double*)malloc(sizeof(double) * (size_t)D);
+  if (!x || !y || !o) {
+    free(x); free(y); free(o);
+    return -1;
+  }
+  int64_t bad_pos = 0, bad_slot = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t t = qsl[b]; t < qsl[b + 1]; ++t) {
+      const int64_t i = t - qsl[b];
+      const int64_t position = seq_lens[b] - (qsl[b + 1] - qsl[b]) + i;
+      if (position < 0 || position >= max_seq) {
+        ++bad_pos;
+        continue;
+      }
+      const int64_t slot = slot_mapping[t];
+      const int cache_it = slot >= 0 && slot < num_blocks * block_size;
+      if (slot >= num_blocks * block_size) ++bad_slot;
+      const int64_t blk = cache_it ? slot / block_size : 0, off = cache_it ? slot % block_size : 0;
+      for (int64_t h = 0; h < nq + nk + nv; ++h) {
+        /* split: head h of qkv */
+        for (int64_t j = 0; j < D; ++j) x[j] = load_elem(qkv, dt, t * W + h * D + j);
+        if (h >= nq + nk) { /* V: stored as is */
+          if (cache_it) {
+            const int64_t vh = h - nq - nk;
+            for (int64_t j = 0; j < D; ++j)
+              store_elem(v_cache, dt, ((blk * nv + vh) * block_size + off) * D + j, x[j]);
+          }
+          continue;
+        }
+        /* RMSNorm over the head */
+        const void* gamma = h < nq ? q_gamma : k_gamma;
+        double ss = 0.0;
+        for (int64_t j = 0; j < D; ++j) ss += x[j] * x[j];
+        const double inv = 1.0 / sqrt(ss / (double)D + eps);
+        for (int64_t j = 0; j < D; ++j) y[j] = x[j] * inv * load_elem(gamma, dt, j);
+        /* RoPE: concat(low*cos - high*sin, high*cos + low*sin) */
+        for (int64_t j = 0; j < half; ++j) {
+          const double c = load_elem(cache, dt, position * D + j);
+          const double s = load_elem(cache, dt, position * D + half + j);
+          o[j] = y[j] * c - y[half + j] * s;
+          o[half + j] = y[half + j] * c + y[j] * s;
+        }
+        if (h < nq) {
+          for (int64_t j = 0; j < D; ++j) store_elem(q_out, dt, (t * nq + h) * D + j, o[j]);
+        } else if (cache_it) {
+          const int64_t kh = h - nq;
+          for (int64_t j = 0; j < D; ++j)
+            store_elem(k_cache, dt, ((blk * nk + kh) * block_size + off) * D + j, o[j]);
+        }
+      }
+    }
+  }
+  free(x); free(y); free(o);
+  return bad_pos + (bad_slot << 32);
+}

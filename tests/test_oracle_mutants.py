@@ -50,6 +50,22 @@ MUTANTS = [
     ("interleaved splice: row 1 stride start off by one",
      "for (int64_t i = 1; i < 3 * mrope_section[1] && i < half; i += 3) {",
      "for (int64_t i = 0; i < 3 * mrope_section[1] && i < half; i += 3) {"),
+    ("fused: mean over D - 1",
+     "const double inv = 1.0 / sqrt(ss / (double)D + eps);",
+     "const double inv = 1.0 / sqrt(ss / (double)(D - 1) + eps);"),
+    ("fused: gamma index shifted",
+     "for (int64_t j = 0; j < D; ++j) y[j] = x[j] * inv * load_elem(gamma, dt, j);",
+     "for (int64_t j = 0; j < D; ++j) y[j] = x[j] * inv * load_elem(gamma, dt, (j + 1) % D);"),
+    ("fused: q gamma for k",
+     "const void* gamma = h < nq ? q_gamma : k_gamma;", "const void* gamma = q_gamma;"),
+    ("fused: rope sign",
+     "o[j] = y[j] * c - y[half + j] * s;", "o[j] = y[j] * c + y[half + j] * s;"),
+    ("fused: block and offset swapped",
+     "const int64_t blk = cache_it ? slot / block_size : 0, off = cache_it ? slot % block_size : 0;",
+     "const int64_t blk = cache_it ? slot % block_size : 0, off = cache_it ? slot / block_size : 0;"),
+    ("fused: position off by one",
+     "const int64_t position = seq_lens[b] - (qsl[b + 1] - qsl[b]) + i;",
+     "const int64_t position = seq_lens[b] - (qsl[b + 1] - qsl[b]) + i + 1;"),
     ("rounding ties away from zero",
      "double m = nearbyint(ldexp(a, (f.p - 1) - E));", "double m = round(ldexp(a, (f.p - 1) - E));"),
     ("rounding by truncation",

@@ -636,3 +636,103 @@ def test_interleaved_cache_mode_matches_complex_form(section):
         z = (h[..., :half] + 1j * h[..., half:]) * (cos + 1j * sin)[:, None, :]
         ref = np.concatenate([z.real, z.imag], axis=-1).reshape(23, -1)
         assert _ulp_dist(got, oracle.round_to(ref, torch.float32)).max() <= 1
+
+
+# ----------------------------------------------------------------------------
+# fused QKV split + RMSNorm + RoPE + paged cache write
+# ----------------------------------------------------------------------------
+
+def test_qkv_hand_case():
+    g = _load("qkv_rmsnorm_rope_cache_hand_case.json")
+    f = torch.float32
+    cache = torch.zeros(g["cache_rows"], 2)
+    for p in range(g["cache_rows"]):
+        cache[p, 0], cache[p, 1] = p / 8, 0.25
+    q_out = torch.full((3, 2), 99.0)
+    k_cache = torch.full((g["num_blocks"], 1, g["block_size"], 2), 99.0)
+    v_cache = torch.full_like(k_cache, 99.0)
+    qo, kc, vc, bp, bs = oracle.qkv_rmsnorm_rope_cache(
+        torch.tensor(g["qkv"], dtype=f), 1, 1, 1, torch.tensor(g["q_gamma"], dtype=f),
+        torch.tensor(g["k_gamma"], dtype=f), 0.0, cache, torch.tensor(g["seq_lens"]),
+        torch.tensor(g["query_start_loc"]), torch.tensor(g["slot_mapping"]), q_out, k_cache, v_cache)
+    assert bp == 0 and bs == 0
+    assert qo.tolist() == g["q_out"]
+    want_k = torch.full_like(k_cache, 99.0)
+    want_v = torch.full_like(v_cache, 99.0)
+    for w in g["k_cache_writes"]:
+        want_k[w["block"], 0, w["offset"]] = torch.tensor(w["value"])
+    for w in g["v_cache_writes"]:
+        want_v[w["block"], 0, w["offset"]] = torch.tensor(w["value"])
+    assert torch.equal(kc, want_k) and torch.equal(vc, want_v)
+
+
+def _qkv_reference(case):
+    """Independent float64 composition: torch's rms_norm (a library routine),
+    the textbook complex-number rotation, a scatter by slot; positions from
+    the page's formula.  Returns (q_out, k_cache, v_cache) before rounding."""
+    T, D = case.tokens, case.head_size
+    x = case.qkv.double().reshape(T, -1, D)
+    nq, nk = case.nq, case.nk
+    q = torch.nn.functional.rms_norm(x[:, :nq], (D,), case.q_gamma.double(), case.eps)
+    k = torch.nn.functional.rms_norm(x[:, nq:nq + nk], (D,), case.k_gamma.double(), case.eps)
+    v = x[:, nq + nk:]
+    pos = torch.cat([torch.arange(case.query_start_loc[b + 1] - case.query_start_loc[b]) + case.seq_lens[b]
+                     - (case.query_start_loc[b + 1] - case.query_start_loc[b]) for b in range(len(case.seq_lens))])
+    tab = case.cache.double()[pos]
+    w = (tab[:, :D // 2] + 1j * tab[:, D // 2:])[:, None, :]
+
+    def rot(y):
+        z = (y[..., :D // 2] + 1j * y[..., D // 2:]).numpy() * w.numpy()
+        return np.concatenate([z.real, z.imag], axis=-1)
+
+    qo = rot(q).reshape(T, -1)
+    kc = case.k_cache.double().numpy().copy()
+    vc = case.v_cache.double().numpy().copy()
+    kr, vr = rot(k), v.numpy()
+    bs = case.k_cache.shape[2]
+    for t in range(T):
+        s = int(case.slot_mapping[t])
+        if s < 0:
+            continue
+        kc[s // bs, :, s % bs] = kr[t]
+        vc[s // bs, :, s % bs] = vr[t]
+    return qo, kc, vc
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_qkv_matches_independent_composition(dt):
+    case = W.qkv_case("t", 31, [5, 1, 3, 1], [2, 9, 0, 20], 3, 2, 2, 32, 4, dt, pad_every=4)
+    qo, kc, vc, bp, bs = oracle.qkv_rmsnorm_rope_cache(
+        case.qkv, case.nq, case.nk, case.nv, case.q_gamma, case.k_gamma, case.eps, case.cache, case.seq_lens,
+        case.query_start_loc, case.slot_mapping, case.q_out, case.k_cache, case.v_cache)
+    assert bp == 0 and bs == 0
+    rq, rk, rv = _qkv_reference(case)
+    # one rounding on each side of a float64 computation: within one ulp
+    assert _ulp_dist(qo, oracle.round_to(rq, dt)).max() <= 1
+    assert _ulp_dist(kc, oracle.round_to(rk, dt)).max() <= 1
+    assert _same_bits(vc, oracle.round_to(rv, dt))
+
+
+def test_qkv_identity_rotation_gives_unit_rms_heads():
+    case = W.qkv_case("t", 32, [6], [0], 2, 1, 1, 64, 8, torch.float32)
+    case.cache = torch.cat([torch.ones(case.cache.shape[0], 32), torch.zeros(case.cache.shape[0], 32)], dim=1)
+    case.q_gamma = torch.ones(64)
+    qo, _, _, _, _ = oracle.qkv_rmsnorm_rope_cache(
+        case.qkv, 2, 1, 1, case.q_gamma, case.k_gamma, 0.0, case.cache, case.seq_lens, case.query_start_loc,
+        case.slot_mapping, case.q_out, case.k_cache, case.v_cache)
+    ms = qo.double().reshape(6, 2, 64).pow(2).mean(-1)
+    assert torch.allclose(ms, torch.ones_like(ms), rtol=0, atol=1e-6)
+
+
+def test_qkv_bad_position_and_slot_are_skipped():
+    case = W.qkv_case("t", 33, [2, 2], [3, 3], 1, 1, 1, 32, 4, torch.bfloat16)
+    case.cache = case.cache[:5].contiguous()  # positions 3, 4 valid; batch 1 also 3, 4
+    case.seq_lens = torch.tensor([5, 6])      # batch 1 positions 4, 5: 5 is out of range
+    case.slot_mapping = case.slot_mapping.clone()
+    case.slot_mapping[0] = case.k_cache.shape[0] * case.k_cache.shape[2]  # past the pool
+    qo, kc, vc, bp, bs = oracle.qkv_rmsnorm_rope_cache(
+        case.qkv, 1, 1, 1, case.q_gamma, case.k_gamma, case.eps, case.cache, case.seq_lens, case.query_start_loc,
+        case.slot_mapping, case.q_out, case.k_cache, case.v_cache)
+    assert bp == 1 and bs == 1
+    assert _same_bits(qo[3], case.q_out[3])  # bad position: q row unwritten
+    assert not _same_bits(qo[0], case.q_out[0])  # bad slot: q still computed

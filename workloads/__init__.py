@@ -159,8 +159,8 @@ def inplace_case(name: str, seed: int, shape: Sequence[int], start: int, end: in
                  base: float = 10000.0, cs_kind: str = "rotary") -> InplaceCase:
     """x ~ N(0,1) of ``shape``; cos/sin of ``cs_shape`` (default [1,S,1,L]).
 
-    ``cs_kind='rotary'``: the position of a cos/sin row is its flat index along
-    the non-broadcast (B, S, N) dims taken in S-major order, i.e. s for the
+    ``cs_kind='rotary'``: cos/sin row r (flat index over the first three dims
+    of ``cs_shape``) is the rotation of position r, i.e. position s for the
     [1,S,1,L] layout.  ``cs_kind='randn'``: cos/sin are free N(0,1) tensors.
     """
     B, S, N, D = shape
@@ -253,3 +253,76 @@ def mrope_neox_bf16() -> CacheCase:
     pos = mrope_positions()
     return cache_case("mrope_neox_bf16_32768tok_28q4k_h128_s16_24_24", 4, pos.shape[1], 28, 4, 128, 128,
                       40960, torch.bfloat16, True, base=1e6, positions=pos, mrope_section=[16, 24, 24])
+
+
+# --------------------------------------------------------------------------
+# Fused QKV split + RMSNorm + RoPE + paged KV-cache write
+# --------------------------------------------------------------------------
+
+@dataclass
+class QkvCase:
+    """Inputs of the fused QKV operator; q_out/k_cache/v_cache hold the initial
+    contents (sentinel values that unwritten entries keep)."""
+    name: str
+    qkv: torch.Tensor
+    nq: int
+    nk: int
+    nv: int
+    q_gamma: torch.Tensor
+    k_gamma: torch.Tensor
+    eps: float
+    cache: torch.Tensor
+    seq_lens: torch.Tensor
+    query_start_loc: torch.Tensor
+    slot_mapping: torch.Tensor
+    q_out: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+
+    @property
+    def tokens(self) -> int:
+        return int(self.qkv.shape[0])
+
+    @property
+    def head_size(self) -> int:
+        return int(self.qkv.shape[1]) // (self.nq + self.nk + self.nv)
+
+
+def qkv_case(name: str, seed: int, query_lens: Sequence[int], context_lens: Sequence[int], nq: int, nk: int,
+             nv: int, head_size: int, block_size: int, dtype: torch.dtype, base: float = 10000.0,
+             eps: float = 1e-6, pad_every: int = 0) -> QkvCase:
+    """Batches with ``query_lens[b]`` new tokens on top of ``context_lens[b]``
+    cached ones (seqLens = context + query).  Every token gets a distinct cache
+    slot drawn at random from the pool (its KV blocks), except that with
+    ``pad_every`` > 0 every pad_every-th token gets slot -1 (padding)."""
+    T = int(sum(query_lens))
+    seq_lens = torch.tensor([c + q for c, q in zip(context_lens, query_lens)], dtype=torch.int64)
+    qsl = torch.tensor([0] + list(np.cumsum(query_lens)), dtype=torch.int64)
+    W = (nq + nk + nv) * head_size
+    qkv = normal(stream_seed(seed, 0), (T, W), dtype)
+    g = normal(stream_seed(seed, 1), (2, head_size), torch.float32)
+    q_gamma = (1.0 + 0.25 * g[0]).to(dtype)
+    k_gamma = (1.0 + 0.25 * g[1]).to(dtype)
+    max_seq = int(seq_lens.max()) + 1
+    cache = cos_sin_cache(max_seq, head_size, base, dtype)
+    num_blocks = (T + block_size - 1) // block_size + 1
+    u = uniform(stream_seed(seed, 2), num_blocks * block_size)
+    slots = torch.from_numpy(np.argsort(u, kind="stable")[:T].astype(np.int64))
+    if pad_every:
+        slots[::pad_every] = -1
+    q_out = torch.full((T, nq * head_size), 3.0, dtype=dtype)
+    k_cache = torch.full((num_blocks, nk, block_size, head_size), 5.0, dtype=dtype)
+    v_cache = torch.full((num_blocks, nv, block_size, head_size), 7.0, dtype=dtype)
+    return QkvCase(name, qkv, nq, nk, nv, q_gamma, k_gamma, eps, cache, seq_lens, qsl, slots, q_out, k_cache,
+                   v_cache)
+
+
+def qkv_rmsnorm_rope_bf16() -> QkvCase:
+    """Mixed prefill/decode batch: 4 prefill chunks of 1920 tokens after 4096
+    cached ones, then 512 decode requests with 100..8000 cached tokens; 32 q,
+    8 k, 8 v heads of 128; bf16; 128-token KV blocks; seed 5."""
+    ctx_dec = (100 + uniform_int(stream_seed(5, 3), 512, 0, 7900)).tolist()
+    query_lens = [1920] * 4 + [1] * 512
+    context_lens = [4096] * 4 + ctx_dec
+    return qkv_case("qkv_rmsnorm_rope_bf16_8192tok_32q8k8v_h128", 5, query_lens, context_lens, 32, 8, 8, 128,
+                    128, torch.bfloat16)
