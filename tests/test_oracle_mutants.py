@@ -1,5 +1,8 @@
 """Plant plausible mistakes in a copy of the oracle (on the CPU) and check that
-the pins in ``test_oracle_pins.py`` catch every one of them."""
+the pins in ``test_oracle_pins.py`` catch every one of them.
+
+Every planted mistake keeps all memory accesses inside their buffers, so a
+mutant can only compute wrong values, never corrupt the test process."""
 import os
 
 import pytest
@@ -60,9 +63,9 @@ MUTANTS = [
      "const void* gamma = h < nq ? q_gamma : k_gamma;", "const void* gamma = q_gamma;"),
     ("fused: rope sign",
      "o[j] = y[j] * c - y[half + j] * s;", "o[j] = y[j] * c + y[half + j] * s;"),
-    ("fused: block and offset swapped",
+    ("fused: cache offset off by one (stays inside the block)",
      "const int64_t blk = cache_it ? slot / block_size : 0, off = cache_it ? slot % block_size : 0;",
-     "const int64_t blk = cache_it ? slot % block_size : 0, off = cache_it ? slot / block_size : 0;"),
+     "const int64_t blk = cache_it ? slot / block_size : 0, off = cache_it ? (slot + 1) % block_size : 0;"),
     ("fused: position off by one",
      "const int64_t position = seq_lens[b] - (qsl[b + 1] - qsl[b]) + i;",
      "const int64_t position = seq_lens[b] - (qsl[b + 1] - qsl[b]) + i + 1;"),
