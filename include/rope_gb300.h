@@ -8,6 +8,7 @@
  *   rope_with_sin_cos_cache(_v2)  cos/sin-cache-indexed RoPE of query and key (rope /
  *                                 mrope, GPT-NeoX or GPT-J style; V2: interleaved mrope
  *                                 splice, strided inputs, separate outputs)
+ *   rope_qkv_rmsnorm_rope_cache   fused QKV split + RMSNorm + RoPE + paged KV-cache write
  *
  * Sources (web pages, cited by title and section):
  *  [IPRM] "CANN ops-transformer 的 aclnnInplacePartialRotaryMul 算子：Inplace
@@ -45,7 +46,7 @@
 extern "C" {
 #endif
 
-#define ROPE_ABI_VERSION 3
+#define ROPE_ABI_VERSION 4
 
 typedef enum {
   ROPE_F32 = 0,  /* IEEE binary32 */
@@ -72,7 +73,8 @@ enum {
 /* Codes reported by rope_get_device_error. */
 enum {
   ROPE_DEVICE_OK = 0,
-  ROPE_DEVICE_POSITION_OUT_OF_RANGE = 1 /* some position was < 0 or >= maxSeqLen */
+  ROPE_DEVICE_POSITION_OUT_OF_RANGE = 1, /* some position was < 0 or >= maxSeqLen */
+  ROPE_DEVICE_SLOT_OUT_OF_RANGE = 2      /* some KV-cache slot was >= blocks * block size */
 };
 
 /*
@@ -192,6 +194,45 @@ int rope_with_sin_cos_cache_v2(const rope_tensor_t* positions, const rope_tensor
                                const int64_t* mrope_section, int64_t mrope_section_len, int32_t cache_mode,
                                int64_t query_row_stride, int64_t key_row_stride, const rope_tensor_t* query_out,
                                const rope_tensor_t* key_out, void* stream);
+
+/*
+ * Fused QKV split + RMSNorm + RoPE + paged KV-cache write.
+ * ["aclnnQkvRmsNormRopeCacheWithKScale" page, section 计算公式; its FP8
+ *  quantisation and optional rotation matmul are not part of this call]
+ *
+ * Per token t of batch b (t in [query_start_loc[b], query_start_loc[b+1])):
+ *   position = seq_lens[b] - (query_start_loc[b+1] - query_start_loc[b]) + (t - query_start_loc[b])
+ *   cos, sin = the two halves of cos_sin_cache[position]
+ *   for each of the Nq + Nk + Nv heads x of qkv[t] (D elements each):
+ *     q and k heads:  y = x / sqrt(mean(x^2) + eps) * gamma   (q_gamma or k_gamma)
+ *                     r = concat(y_lo*cos - y_hi*sin, y_hi*cos + y_lo*sin)
+ *     q_out[t, h] = r;  k_cache[slot/BS, h, slot%BS, :] = r;  v_cache[slot/BS, h, slot%BS, :] = x (v heads)
+ *   with slot = slot_mapping[t] and BS the cache block size.
+ *
+ *   qkv            [T, (Nq + Nk + Nv) * D]; F32, F16 or BF16; D a multiple of 32 (F16/BF16)
+ *                  or 16 (F32), at most 512 (F16/BF16) or 256 (F32).
+ *   q_gamma, k_gamma  [D], same dtype.      eps >= 0 (added to the mean of squares).
+ *   cos_sin_cache  [maxSeq, D], same dtype: cos in the first half of a row, sin in the second.
+ *   seq_lens       I64 [B]: tokens of each sequence including this call's;
+ *   query_start_loc I64 [B + 1]: first token of each batch in qkv (last entry T);
+ *   slot_mapping   I64 [T]: cache slot of each token; a negative slot writes no cache
+ *                  (padding).
+ *   q_out          [T, Nq * D] output; k_cache [NB, Nk, BS, D] and v_cache [NB, Nv, BS, D]
+ *                  are updated in place at the tokens' slots only.
+ * All float tensors 16-byte aligned, int64 tensors 8-byte aligned, all contiguous.
+ * Computed in binary32 (mean of squares, reciprocal square root, products, the
+ * rotation as in rope_with_sin_cos_cache) and rounded once per output element.
+ * A token whose position falls outside the table writes nothing and records
+ * ROPE_DEVICE_POSITION_OUT_OF_RANGE; a slot at or past NB * BS writes no cache and
+ * records ROPE_DEVICE_SLOT_OUT_OF_RANGE (q_out is still written).
+ * Returns ROPE_OK, ROPE_ERR_PARAM_NULLPTR, ROPE_ERR_PARAM_INVALID or ROPE_ERR_CUDA.
+ */
+int rope_qkv_rmsnorm_rope_cache(const rope_tensor_t* qkv, int64_t num_q_heads, int64_t num_k_heads,
+                                int64_t num_v_heads, const rope_tensor_t* q_gamma, const rope_tensor_t* k_gamma,
+                                float eps, const rope_tensor_t* cos_sin_cache, const rope_tensor_t* seq_lens,
+                                const rope_tensor_t* query_start_loc, const rope_tensor_t* slot_mapping,
+                                const rope_tensor_t* q_out, const rope_tensor_t* k_cache,
+                                const rope_tensor_t* v_cache, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device-side error word of the

@@ -70,3 +70,31 @@ def assert_matches(got: torch.Tensor, ref: torch.Tensor, what: str = "") -> dict
     res = compare(got, ref)
     assert res["ok"], "%s: %s" % (what, res)
     return res
+
+
+def ulp_of(ref: torch.Tensor) -> np.ndarray:
+    """One unit in the last place of each element of ``ref`` (its own dtype)."""
+    r = ref.detach().cpu().float().abs().double().numpy()
+    bits = {torch.float32: 24, torch.float16: 11, torch.bfloat16: 8}[ref.dtype]
+    emin = {torch.float32: -126, torch.float16: -14, torch.bfloat16: -126}[ref.dtype]
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(r > 0, r, 1.0)))
+    e = np.maximum(e, emin)
+    return np.ldexp(1.0, (e - (bits - 1)).astype(np.int64))
+
+
+def assert_close_scaled(got: torch.Tensor, ref: torch.Tensor, scale: np.ndarray, rel: float, what: str = ""):
+    """|got - ref| <= 1 ulp(ref) + rel * scale, elementwise (NaN matches NaN).
+
+    For results computed from intermediates that already carry binary32
+    rounding (e.g. a normalisation before a rotation), ``scale`` is the size of
+    the terms that cancel, so the bound does not blow up under cancellation."""
+    g = got.detach().cpu().double().numpy()
+    r = ref.detach().cpu().double().numpy()
+    both_nan = np.isnan(g) & np.isnan(r)
+    with np.errstate(invalid="ignore"):
+        err = np.abs(g - r)
+    bound = ulp_of(ref) + rel * np.broadcast_to(scale, r.shape)
+    bad = ~(both_nan | (err <= bound))
+    assert not bad.any(), "%s: %d elements out of bound, worst excess %g" % (
+        what, int(bad.sum()), float(np.nanmax(np.where(bad, err - bound, 0))))

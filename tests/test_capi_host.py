@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.rope_abi_version() == 3
+    assert lib.rope_abi_version() == 4
     for st in (C.ROPE_OK, C.ROPE_ERR_PARAM_NULLPTR, C.ROPE_ERR_PARAM_INVALID, C.ROPE_ERR_CUDA, 12345):
         s = C.status_string(st)
         assert isinstance(s, str) and s
@@ -258,3 +258,37 @@ def test_cache_v2_rejections(lib, case, status):
     args.update(case)
     pos, q, k, c = args.pop("pos"), args.pop("q"), args.pop("k"), args.pop("c")
     assert _v2(lib, pos, q, k, c, **args) == status
+
+
+def _qkv(lib, **over):
+    T, nq, nk, nv, D, NB, BS, B = 6, 2, 1, 1, 64, 3, 4, 2
+    t = dict(qkv=_d(C.BF16, (T, (nq + nk + nv) * D)), qg=_d(C.BF16, (D,)), kg=_d(C.BF16, (D,)),
+             cache=_d(C.BF16, (50, D)), sl=_d(C.I64, (B,)), qsl=_d(C.I64, (B + 1,)), slots=_d(C.I64, (T,)),
+             qo=_d(C.BF16, (T, nq * D)), kc=_d(C.BF16, (NB, nk, BS, D)), vc=_d(C.BF16, (NB, nv, BS, D)),
+             nq=nq, nk=nk, nv=nv, eps=1e-6)
+    t.update(over)
+    ref = lambda x: ctypes.byref(x) if x is not None else None  # noqa: E731
+    return lib.rope_qkv_rmsnorm_rope_cache(ref(t["qkv"]), t["nq"], t["nk"], t["nv"], ref(t["qg"]), ref(t["kg"]),
+                                           t["eps"], ref(t["cache"]), ref(t["sl"]), ref(t["qsl"]), ref(t["slots"]),
+                                           ref(t["qo"]), ref(t["kc"]), ref(t["vc"]), None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(qkv=None), C.ROPE_ERR_PARAM_NULLPTR),
+    (dict(vc=None), C.ROPE_ERR_PARAM_NULLPTR),
+    (dict(qg=_d(C.F16, (64,))), C.ROPE_ERR_PARAM_INVALID),          # gamma dtype
+    (dict(sl=_d(C.F32, (2,))), C.ROPE_ERR_PARAM_INVALID),           # seq_lens not int64
+    (dict(nq=3), C.ROPE_ERR_PARAM_INVALID),                         # heads do not divide the width
+    (dict(qkv=_d(C.BF16, (6, 4 * 48)), qg=_d(C.BF16, (48,)), kg=_d(C.BF16, (48,))), C.ROPE_ERR_PARAM_INVALID),
+    (dict(qkv=_d(C.BF16, (6, 4 * 1024)), qg=_d(C.BF16, (1024,)), kg=_d(C.BF16, (1024,))), C.ROPE_ERR_PARAM_INVALID),
+    (dict(cache=_d(C.BF16, (50, 32))), C.ROPE_ERR_PARAM_INVALID),   # cache width != D
+    (dict(qsl=_d(C.I64, (2,))), C.ROPE_ERR_PARAM_INVALID),          # query_start_loc length != B + 1
+    (dict(slots=_d(C.I64, (5,))), C.ROPE_ERR_PARAM_INVALID),        # one slot per token
+    (dict(qo=_d(C.BF16, (6, 64))), C.ROPE_ERR_PARAM_INVALID),       # q_out width
+    (dict(vc=_d(C.BF16, (3, 1, 8, 64))), C.ROPE_ERR_PARAM_INVALID),  # block sizes differ
+    (dict(eps=-1.0), C.ROPE_ERR_PARAM_INVALID),
+    (dict(eps=float("nan")), C.ROPE_ERR_PARAM_INVALID),
+    (dict(qkv=_d(C.BF16, (6, 256), FAKE + 8)), C.ROPE_ERR_PARAM_INVALID),  # misaligned
+])
+def test_qkv_rejections(lib, over, status):
+    assert _qkv(lib, **over) == status

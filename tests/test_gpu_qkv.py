@@ -1,0 +1,107 @@
+"""Parity of the fused QKV split + RMSNorm + RoPE + paged cache write.
+
+Tolerance: the q/k outputs are rotations of RMS-normalised values that the
+kernel forms in binary32 (mean of squares over the head, reciprocal square
+root, two products), so their error is relative to the size of the rotated
+terms, not to the result: |got - ref| <= 1 ulp + 8e-6 * 2 * max|y| over the
+head (y the normalised values, computed here in float64 for the bound only).
+V is copied and must be bit-exact, as must every cache entry the call does not
+own and the untouched q_out rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import transformer_rope_positional_gb300 as R
+import workloads as W
+from parity import assert_close_scaled, same_bits
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = [torch.float32, torch.float16, torch.bfloat16]
+REL = 8e-6
+
+
+def _run_gpu(case):
+    d = lambda t: t.cuda()  # noqa: E731
+    qo, kc, vc = d(case.q_out), d(case.k_cache), d(case.v_cache)
+    R.qkv_rmsnorm_rope_cache(d(case.qkv), case.nq, case.nk, case.nv, d(case.q_gamma), d(case.k_gamma), case.eps,
+                             d(case.cache), d(case.seq_lens), d(case.query_start_loc), d(case.slot_mapping), qo, kc,
+                             vc)
+    torch.cuda.synchronize()
+    return qo.cpu(), kc.cpu(), vc.cpu()
+
+
+def _run_oracle(case):
+    return oracle.qkv_rmsnorm_rope_cache(case.qkv, case.nq, case.nk, case.nv, case.q_gamma, case.k_gamma,
+                                         case.eps, case.cache, case.seq_lens, case.query_start_loc,
+                                         case.slot_mapping, case.q_out, case.k_cache, case.v_cache)
+
+
+def _head_scales(case, heads, gamma):
+    """2 * max |normalised value| per (token, head) of the given head range."""
+    D = case.head_size
+    x = case.qkv.double().reshape(case.tokens, -1, D)[:, heads]
+    y = torch.nn.functional.rms_norm(x, (D,), gamma.double(), case.eps)
+    return (2 * y.abs().amax(-1, keepdim=True)).numpy()
+
+
+def _check(case, got, ref):
+    qg, kg, vg = got
+    qr, kr, vr, bp, bs = ref
+    nq, nk, D, T = case.nq, case.nk, case.head_size, case.tokens
+    sq = _head_scales(case, slice(0, nq), case.q_gamma)
+    assert_close_scaled(qg.view(T, nq, D), qr.view(T, nq, D), sq, REL, "q_out")
+    # k: compare cache entries; owned entries within bound, the rest bit-exact
+    sk = _head_scales(case, slice(nq, nq + nk), case.k_gamma)
+    scale = np.zeros(kr.shape[:3] + (1,))
+    bsz = case.k_cache.shape[2]
+    for t in range(T):
+        s = int(case.slot_mapping[t])
+        if 0 <= s < kr.shape[0] * bsz:
+            scale[s // bsz, :, s % bsz] = sk[t]
+    assert_close_scaled(kg, kr, scale, REL, "k_cache")
+    assert same_bits(vg, vr)
+    return bp, bs
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("D", [64, 96, 128, 256])
+def test_head_sizes_and_dtypes(rope_gpu, dt, D):
+    case = W.qkv_case("qkv", 131, [37, 1, 1, 64, 3], [0, 100, 5, 30, 2000], 4, 2, 2, D, 16, dt, pad_every=7)
+    bp, bs = _check(case, _run_gpu(case), _run_oracle(case))
+    assert bp == 0 and bs == 0 and R.get_device_error() == 0
+
+
+@pytest.mark.parametrize("heads", [(8, 1, 1), (1, 1, 0), (0, 2, 2), (5, 3, 1)])
+def test_head_counts(rope_gpu, heads):
+    nq, nk, nv = heads
+    case = W.qkv_case("heads", 132, [17, 1, 9], [4, 50, 0], nq, nk, nv, 128, 8, torch.bfloat16)
+    _check(case, _run_gpu(case), _run_oracle(case))
+
+
+def test_mixed_prefill_decode_workload(rope_gpu):
+    case = W.qkv_rmsnorm_rope_bf16()
+    bp, bs = _check(case, _run_gpu(case), _run_oracle(case))
+    assert bp == 0 and bs == 0 and R.get_device_error() == 0
+
+
+def test_bad_position_and_slot(rope_gpu):
+    case = W.qkv_case("bad", 133, [3, 2], [2, 4], 2, 1, 1, 64, 4, torch.float16)
+    case.cache = case.cache[:6].contiguous()        # batch 1 positions 4, 5 valid; 3 valid
+    case.seq_lens = torch.tensor([5, 7])            # batch 1 positions 5, 6: 6 is out of range
+    case.slot_mapping = case.slot_mapping.clone()
+    case.slot_mapping[1] = case.k_cache.shape[0] * case.k_cache.shape[2] + 3
+    got = _run_gpu(case)
+    assert R.get_device_error() == (R.ROPE_DEVICE_POSITION_OUT_OF_RANGE | R.ROPE_DEVICE_SLOT_OUT_OF_RANGE)
+    ref = _run_oracle(case)
+    bp, bs = _check(case, got, ref)
+    assert bp == 1 and bs == 1
+    assert same_bits(got[0][4], case.q_out[4])      # token with the bad position: q row unwritten
+
+
+def test_padding_slots_write_nothing(rope_gpu):
+    case = W.qkv_case("pad", 134, [8], [8], 2, 1, 1, 128, 4, torch.bfloat16, pad_every=1)
+    qg, kg, vg = _run_gpu(case)
+    assert same_bits(kg, case.k_cache) and same_bits(vg, case.v_cache)
+    _check(case, (qg, kg, vg), _run_oracle(case))

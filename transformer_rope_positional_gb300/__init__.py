@@ -26,6 +26,9 @@ from ._capi import (  # noqa: F401
     rope_inplace_partial,
     rope_inplace_partial_backward,
     rope_with_sin_cos_cache,
+    qkv_rmsnorm_rope_cache,
+    prepare_qkv_rmsnorm_rope_cache,
+    ROPE_DEVICE_SLOT_OUT_OF_RANGE,
     status_string,
 )
 
@@ -36,6 +39,7 @@ __all__ = [
     "rope_inplace_partial",
     "rope_inplace_partial_backward",
     "rope_with_sin_cos_cache",
+    "qkv_rmsnorm_rope_cache",
     "get_device_error",
     "launch_count",
     "status_string",

@@ -24,9 +24,10 @@ ROPE_ERR_PARAM_NULLPTR = 161001
 ROPE_ERR_PARAM_INVALID = 161002
 ROPE_ERR_CUDA = 561000
 ROPE_DEVICE_POSITION_OUT_OF_RANGE = 1
+ROPE_DEVICE_SLOT_OUT_OF_RANGE = 2
 
 EXPORTED = ("rope_inplace_partial", "rope_inplace_partial_backward", "rope_with_sin_cos_cache",
-            "rope_with_sin_cos_cache_v2", "rope_get_device_error",
+            "rope_with_sin_cos_cache_v2", "rope_qkv_rmsnorm_rope_cache", "rope_get_device_error",
             "rope_status_string", "rope_launch_count", "rope_abi_version")
 
 
@@ -67,6 +68,9 @@ def load() -> ctypes.CDLL:
                                                ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_int32,
                                                ctypes.c_int64, ctypes.c_int64, P, P, ctypes.c_void_p]
     lib.rope_with_sin_cos_cache_v2.restype = ctypes.c_int
+    lib.rope_qkv_rmsnorm_rope_cache.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P,
+                                                ctypes.c_float, P, P, P, P, P, P, P, ctypes.c_void_p]
+    lib.rope_qkv_rmsnorm_rope_cache.restype = ctypes.c_int
     lib.rope_get_device_error.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.rope_get_device_error.restype = ctypes.c_int
     lib.rope_status_string.argtypes = [ctypes.c_int]
@@ -207,6 +211,43 @@ def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: t
         what = "rope_with_sin_cos_cache_v2"
     if st != ROPE_OK:
         raise RopeError(st, what)
+
+
+def _qkv_args(qkv, num_q_heads, num_k_heads, num_v_heads, q_gamma, k_gamma, eps, cos_sin_cache, seq_lens,
+              query_start_loc, slot_mapping, q_out, k_cache, v_cache, stream):
+    descs = [tensor_desc(t) for t in (qkv, q_gamma, k_gamma, cos_sin_cache, seq_lens, query_start_loc,
+                                      slot_mapping, q_out, k_cache, v_cache)]
+    r = [ctypes.byref(d) for d in descs]
+    args = (r[0], int(num_q_heads), int(num_k_heads), int(num_v_heads), r[1], r[2], float(eps), r[3], r[4], r[5],
+            r[6], r[7], r[8], r[9], _stream_handle(qkv, stream))
+    return args, descs
+
+
+def qkv_rmsnorm_rope_cache(qkv: torch.Tensor, num_q_heads: int, num_k_heads: int, num_v_heads: int,
+                           q_gamma: torch.Tensor, k_gamma: torch.Tensor, eps: float, cos_sin_cache: torch.Tensor,
+                           seq_lens: torch.Tensor, query_start_loc: torch.Tensor, slot_mapping: torch.Tensor,
+                           q_out: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, stream=None) -> None:
+    """Fused QKV split + RMSNorm + RoPE + paged KV-cache write (see the C header)."""
+    lib = load()
+    args, _ = _qkv_args(qkv, num_q_heads, num_k_heads, num_v_heads, q_gamma, k_gamma, eps, cos_sin_cache,
+                        seq_lens, query_start_loc, slot_mapping, q_out, k_cache, v_cache, stream)
+    st = lib.rope_qkv_rmsnorm_rope_cache(*args)
+    if st != ROPE_OK:
+        raise RopeError(st, "rope_qkv_rmsnorm_rope_cache")
+
+
+def prepare_qkv_rmsnorm_rope_cache(qkv: torch.Tensor, num_q_heads: int, num_k_heads: int, num_v_heads: int,
+                                   q_gamma: torch.Tensor, k_gamma: torch.Tensor, eps: float,
+                                   cos_sin_cache: torch.Tensor, seq_lens: torch.Tensor,
+                                   query_start_loc: torch.Tensor, slot_mapping: torch.Tensor, q_out: torch.Tensor,
+                                   k_cache: torch.Tensor, v_cache: torch.Tensor, stream=None) -> "PreparedCall":
+    """:func:`qkv_rmsnorm_rope_cache` with its arguments marshalled once."""
+    lib = load()
+    tensors = (qkv, q_gamma, k_gamma, cos_sin_cache, seq_lens, query_start_loc, slot_mapping, q_out, k_cache,
+               v_cache)
+    args, descs = _qkv_args(qkv, num_q_heads, num_k_heads, num_v_heads, q_gamma, k_gamma, eps, cos_sin_cache,
+                            seq_lens, query_start_loc, slot_mapping, q_out, k_cache, v_cache, stream)
+    return PreparedCall(lib.rope_qkv_rmsnorm_rope_cache, args, (tensors, descs), "rope_qkv_rmsnorm_rope_cache")
 
 
 def get_device_error(stream=None, device=None) -> int:

@@ -239,6 +239,74 @@ int cache_call(const rope_tensor_t* positions, const rope_tensor_t* query, const
   return cuda_status(rope::launch_cache(p, static_cast<cudaStream_t>(stream)));
 }
 
+// Checks of the fused QKV call, then the launch.
+int qkv_call(const rope_tensor_t* qkv, int64_t nq, int64_t nk, int64_t nv, const rope_tensor_t* q_gamma,
+             const rope_tensor_t* k_gamma, float eps, const rope_tensor_t* cache, const rope_tensor_t* seq_lens,
+             const rope_tensor_t* qsl, const rope_tensor_t* slot_mapping, const rope_tensor_t* q_out,
+             const rope_tensor_t* k_cache, const rope_tensor_t* v_cache, void* stream) {
+  const rope_tensor_t* all[] = {qkv, q_gamma, k_gamma, cache, seq_lens, qsl, slot_mapping, q_out, k_cache, v_cache};
+  for (const rope_tensor_t* t : all)
+    if (!t) return ROPE_ERR_PARAM_NULLPTR;
+  for (const rope_tensor_t* t : all)
+    if (!shape_ok(t)) return ROPE_ERR_PARAM_INVALID;
+  // dtypes: one floating type for the data, int64 for the metadata
+  const int32_t dt = qkv->dtype;
+  if (!is_float(dt)) return ROPE_ERR_PARAM_INVALID;
+  for (const rope_tensor_t* t : {q_gamma, k_gamma, cache, q_out, k_cache, v_cache})
+    if (t->dtype != dt) return ROPE_ERR_PARAM_INVALID;
+  for (const rope_tensor_t* t : {seq_lens, qsl, slot_mapping})
+    if (t->dtype != kI64 || t->ndim != 1) return ROPE_ERR_PARAM_INVALID;
+  // shapes
+  if (nq < 0 || nk < 0 || nv < 0 || nq + nk + nv < 1) return ROPE_ERR_PARAM_INVALID;
+  if (qkv->ndim != 2 || qkv->shape[0] < 1 || qkv->shape[1] % (nq + nk + nv)) return ROPE_ERR_PARAM_INVALID;
+  const int64_t T = qkv->shape[0], D = qkv->shape[1] / (nq + nk + nv);
+  const int64_t mult = dt == kF32 ? 16 : 32;
+  const int64_t lanes = D / 2 / (dt == kF32 ? 4 : 8);  // threads per head row
+  if (D < mult || D % mult || lanes > 32) return ROPE_ERR_PARAM_INVALID;
+  if (q_gamma->ndim != 1 || q_gamma->shape[0] != D || k_gamma->ndim != 1 || k_gamma->shape[0] != D)
+    return ROPE_ERR_PARAM_INVALID;
+  if (cache->ndim != 2 || cache->shape[1] != D || cache->shape[0] < 1) return ROPE_ERR_PARAM_INVALID;
+  const int64_t B = seq_lens->shape[0];
+  if (B < 1 || qsl->shape[0] != B + 1 || slot_mapping->shape[0] != T) return ROPE_ERR_PARAM_INVALID;
+  if (q_out->ndim != 2 || q_out->shape[0] != T || q_out->shape[1] != nq * D) return ROPE_ERR_PARAM_INVALID;
+  if (k_cache->ndim != 4 || v_cache->ndim != 4) return ROPE_ERR_PARAM_INVALID;
+  const int64_t NB = k_cache->shape[0], BS = k_cache->shape[2];
+  if (NB < 1 || BS < 1 || k_cache->shape[1] != nk || k_cache->shape[3] != D || v_cache->shape[0] != NB ||
+      v_cache->shape[1] != nv || v_cache->shape[2] != BS || v_cache->shape[3] != D)
+    return ROPE_ERR_PARAM_INVALID;
+  if (!(eps >= 0.0f) || !(eps < 1e30f)) return ROPE_ERR_PARAM_INVALID;
+  for (const rope_tensor_t* t : all)
+    if (!t->data && numel(t) > 0) return ROPE_ERR_PARAM_NULLPTR;
+  for (const rope_tensor_t* t : {qkv, q_gamma, k_gamma, cache, q_out, k_cache, v_cache})
+    if (t->data && !aligned(t->data, 16)) return ROPE_ERR_PARAM_INVALID;
+  for (const rope_tensor_t* t : {seq_lens, qsl, slot_mapping})
+    if (!aligned(t->data, 8)) return ROPE_ERR_PARAM_INVALID;
+
+  rope::QkvProblem p;
+  p.qkv = qkv->data;
+  p.q_gamma = q_gamma->data;
+  p.k_gamma = k_gamma->data;
+  p.cache = cache->data;
+  p.seq_lens = static_cast<const int64_t*>(seq_lens->data);
+  p.query_start_loc = static_cast<const int64_t*>(qsl->data);
+  p.slot_mapping = static_cast<const int64_t*>(slot_mapping->data);
+  p.q_out = q_out->data;
+  p.k_cache = k_cache->data;
+  p.v_cache = v_cache->data;
+  p.dtype = dt;
+  p.T = T;
+  p.B = B;
+  p.nq = nq;
+  p.nk = nk;
+  p.nv = nv;
+  p.D = D;
+  p.max_seq = cache->shape[0];
+  p.num_blocks = NB;
+  p.block_size = BS;
+  p.eps = eps;
+  return cuda_status(rope::launch_qkv(p, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -269,6 +337,16 @@ int rope_with_sin_cos_cache_v2(const rope_tensor_t* positions, const rope_tensor
                                const rope_tensor_t* key_out, void* stream) {
   return cache_call(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_neox, mrope_section,
                     mrope_section_len, cache_mode, query_row_stride, key_row_stride, query_out, key_out, stream);
+}
+
+int rope_qkv_rmsnorm_rope_cache(const rope_tensor_t* qkv, int64_t num_q_heads, int64_t num_k_heads,
+                                int64_t num_v_heads, const rope_tensor_t* q_gamma, const rope_tensor_t* k_gamma,
+                                float eps, const rope_tensor_t* cos_sin_cache, const rope_tensor_t* seq_lens,
+                                const rope_tensor_t* query_start_loc, const rope_tensor_t* slot_mapping,
+                                const rope_tensor_t* q_out, const rope_tensor_t* k_cache,
+                                const rope_tensor_t* v_cache, void* stream) {
+  return qkv_call(qkv, num_q_heads, num_k_heads, num_v_heads, q_gamma, k_gamma, eps, cos_sin_cache, seq_lens,
+                  query_start_loc, slot_mapping, q_out, k_cache, v_cache, stream);
 }
 
 int rope_get_device_error(void* stream, int32_t* code) {

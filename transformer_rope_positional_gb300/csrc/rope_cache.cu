@@ -22,6 +22,7 @@
 // A position outside [0, maxSeqLen) leaves its token untouched and sets bit
 // ROPE_DEVICE_POSITION_OUT_OF_RANGE of the device error word below.
 #include <algorithm>
+#include <mutex>
 
 #include "rope_device.cuh"
 #include "rope_launch.h"
@@ -292,6 +293,23 @@ cudaError_t launch_cache(const CacheProblem& p, cudaStream_t stream) {
     default:
       return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t device_error_address(unsigned int** out) {
+  constexpr int kMaxDevices = 64;
+  static unsigned int* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_device_error);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&addr[dev]), g_device_error);
+    if (e != cudaSuccess) return e;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t* code) {

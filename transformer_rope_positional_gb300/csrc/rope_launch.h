@@ -53,13 +53,37 @@ inline cudaError_t launch_inplace(const InplaceProblem& p, cudaStream_t stream) 
 }
 cudaError_t launch_cache(const CacheProblem& p, cudaStream_t stream);
 
+// Fused QKV split + RMSNorm + RoPE + paged KV-cache write.
+struct QkvProblem {
+  const void* qkv;  // [T, (nq + nk + nv) * D]
+  const void* q_gamma;
+  const void* k_gamma;
+  const void* cache;  // [max_seq, D] cos||sin
+  const int64_t* seq_lens;         // [B]
+  const int64_t* query_start_loc;  // [B + 1]
+  const int64_t* slot_mapping;     // [T]
+  void* q_out;                     // [T, nq * D]
+  void* k_cache;                   // [num_blocks, nk, block_size, D]
+  void* v_cache;                   // [num_blocks, nv, block_size, D]
+  int32_t dtype;
+  int64_t T, B;
+  int64_t nq, nk, nv, D;
+  int64_t max_seq;
+  int64_t num_blocks, block_size;
+  float eps;
+};
+
+cudaError_t launch_qkv(const QkvProblem& p, cudaStream_t stream);
+
 // Threads that work on one head row in the cache kernel, and the most a CTA
 // of that kernel holds.
 int64_t cache_team_threads(const CacheProblem& p);
 int64_t cache_max_team_threads();
 
-// Device error word of the current device.
+// Device error word of the current device: read-and-clear, and its address
+// for kernels of other translation units.
 cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t* code);
+cudaError_t device_error_address(unsigned int** out);
 
 // Launch bookkeeping.
 void count_launch();

@@ -1,0 +1,211 @@
+// Fused QKV split + RMSNorm + RoPE + paged KV-cache write.
+//
+// Operator: the "aclnnQkvRmsNormRopeCacheWithKScale" page, section 计算公式,
+// without its FP8 quantisation and its optional rotation matmul:
+//   q, k, v = split(qkv, [Nq, Nk, Nv])                         (heads of D)
+//   y = x / sqrt(mean(x^2) + eps) * gamma                      (q and k heads)
+//   position = seqLens[b] - (qsl[b+1] - qsl[b]) + i            (token i of batch b)
+//   y_rope = concat(y_low*cos - y_high*sin, y_high*cos + y_low*sin)
+//   q_out[t, h] = y_rope;  kCache[slot/BS, h, slot%BS] = y_rope;  vCache[...] = v
+// cos/sin are the halves of row `position` of a [maxSeq, D] cos||sin table.
+//
+// GB300 design.  Same streaming structure as the other kernels: items of U
+// consecutive heads of one token, row groups of C threads (thread c owns the
+// c-th 16-byte chunk of both halves of a head, the NeoX pairing), persistent
+// grid striding over items.  The RMSNorm reduction is a sum of the thread's
+// 2*VEC squares followed by a butterfly of warp shuffles inside the row group
+// (groups are padded to a power of two lanes), so a head never leaves
+// registers: one read of qkv, one write of q_out or of the cache slot.  The
+// per-token metadata (batch by binary search over queryStartLoc, position,
+// slot) is computed once per item.  Positions outside the table and slots past
+// the pool set bits of the device error word and skip the writes.
+#include <algorithm>
+
+#include "rope_device.cuh"
+#include "rope_launch.h"
+
+namespace rope {
+namespace {
+
+#ifndef ROPE_QKV_ROWS_IN_FLIGHT
+#define ROPE_QKV_ROWS_IN_FLIGHT 4
+#endif
+#ifndef ROPE_QKV_THREADS
+#define ROPE_QKV_THREADS 128
+#endif
+constexpr int kRowsInFlight = ROPE_QKV_ROWS_IN_FLIGHT;
+constexpr int kThreads = ROPE_QKV_THREADS;
+constexpr unsigned kPositionOutOfRange = 1u;
+constexpr unsigned kSlotOutOfRange = 2u;
+
+struct QkvArgs {
+  int64_t T, B;
+  int64_t max_seq;
+  int64_t W;          // qkv row width, (nq + nk + nv) * D
+  int64_t num_slots;  // num_blocks * block_size
+  int64_t items;      // T * head_chunks
+  int32_t nq, nk, nv;
+  int32_t D;
+  int32_t block_size;
+  int32_t chunks;       // C: active threads per head row
+  int32_t group;        // C rounded up to a power of two (lanes per row group)
+  int32_t head_chunks;  // ceil(H / U)
+  float eps;
+  float inv_d;
+};
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kThreads)
+    qkv_kernel(const T* __restrict__ qkv, const T* __restrict__ q_gamma, const T* __restrict__ k_gamma,
+               const T* __restrict__ cache, const int64_t* __restrict__ seq_lens, const int64_t* __restrict__ qsl,
+               const int64_t* __restrict__ slot_mapping, T* __restrict__ q_out, T* __restrict__ k_cache,
+               T* __restrict__ v_cache, unsigned int* __restrict__ err, QkvArgs a) {
+  constexpr int U = kRowsInFlight;
+  const int G = a.group;
+  const int P = blockDim.x / G;  // row groups per CTA
+  const int g = threadIdx.x / G;
+  const int c = threadIdx.x - g * G;
+  const bool active = c < a.chunks;  // padding lanes only join the reduction
+  const int lane = threadIdx.x & 31;
+  const unsigned gmask = (G >= 32 ? 0xffffffffu : ((1u << G) - 1u)) << (lane & ~(G - 1));
+  const int half = a.D / 2;
+  const int i0 = (active ? c : 0) * VEC;
+  const int H = a.nq + a.nk + a.nv;
+  wait_for_prior_grid();
+
+  // gamma of this thread's elements, both branches, both halves
+  Vec<T, VEC> gq1, gq2, gk1, gk2;
+  load_vec<false>(gq1, q_gamma + i0);
+  load_vec<false>(gq2, q_gamma + half + i0);
+  load_vec<false>(gk1, k_gamma + i0);
+  load_vec<false>(gk2, k_gamma + half + i0);
+
+  for (int64_t item = (int64_t)blockIdx.x * P + g; item < a.items; item += (int64_t)gridDim.x * P) {
+    const int64_t t = item / a.head_chunks;
+    const int h0 = (int)(item - t * a.head_chunks) * U;
+    const int n = min(U, H - h0);
+    // ---- issue the loads of the item's head rows
+    Vec<T, VEC> x1[U], x2[U];
+    const T* src = qkv + t * a.W + (int64_t)h0 * a.D;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (u < n && active) {
+        load_vec<true>(x1[u], src + u * a.D + i0);
+        load_vec<true>(x2[u], src + u * a.D + half + i0);
+      }
+    // ---- token metadata: batch (largest b with qsl[b] <= t), position, slot
+    int64_t lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi + 1) / 2;
+      if (__ldg(qsl + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    const int64_t start = __ldg(qsl + lo), qlen = __ldg(qsl + lo + 1) - start;
+    const int64_t position = __ldg(seq_lens + lo) - qlen + (t - start);
+    const int64_t slot = __ldg(slot_mapping + t);
+    const bool pos_ok = position >= 0 && position < a.max_seq;
+    const bool cache_it = slot >= 0 && slot < a.num_slots;
+    if (c == 0 && h0 == 0) {  // reported once per token
+      if (!pos_ok) atomicOr(err, kPositionOutOfRange);
+      else if (slot >= a.num_slots) atomicOr(err, kSlotOutOfRange);
+    }
+    if (!pos_ok) continue;  // nothing of this token is written
+    float cf[VEC], sf[VEC];
+    load_f32<T, VEC>(cf, cache + position * a.D + i0);
+    load_f32<T, VEC>(sf, cache + position * a.D + half + i0);
+    const int64_t blk = cache_it ? slot / a.block_size : 0, off = cache_it ? slot % a.block_size : 0;
+
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (u >= n) break;
+      const int h = h0 + u;
+      if (h >= a.nq + a.nk) {  // V: stored as is
+        if (cache_it && active) {
+          T* dst = v_cache + ((blk * a.nv + (h - a.nq - a.nk)) * a.block_size + off) * a.D;
+          store_vec(dst + i0, x1[u]);
+          store_vec(dst + half + i0, x2[u]);
+        }
+        continue;
+      }
+      // RMSNorm: this thread's squares, then a butterfly inside the row group
+      float ss = 0.f;
+      if (active) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const float v1 = widen(x1[u].e[e]), v2 = widen(x2[u].e[e]);
+          ss = __fmaf_rn(v1, v1, ss);
+          ss = __fmaf_rn(v2, v2, ss);
+        }
+      }
+      for (int m = G / 2; m > 0; m /= 2) ss += __shfl_xor_sync(gmask, ss, m, G);
+      const float inv = rsqrtf(__fmaf_rn(ss, a.inv_d, a.eps));
+      if (!active) continue;
+      const bool is_q = h < a.nq;
+      T* dst = is_q ? q_out + (t * a.nq + h) * (int64_t)a.D
+                    : (cache_it ? k_cache + ((blk * a.nk + (h - a.nq)) * a.block_size + off) * a.D : nullptr);
+      if (dst == nullptr) continue;
+      const Vec<T, VEC>& g1 = is_q ? gq1 : gk1;
+      const Vec<T, VEC>& g2 = is_q ? gq2 : gk2;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const float y1 = __fmul_rn(__fmul_rn(widen(x1[u].e[e]), inv), widen(g1.e[e]));
+        const float y2 = __fmul_rn(__fmul_rn(widen(x2[u].e[e]), inv), widen(g2.e[e]));
+        x1[u].e[e] = narrow<T>(diff_of_products(y1, cf[e], y2, sf[e]));
+        x2[u].e[e] = narrow<T>(diff_of_products(y2, cf[e], -y1, sf[e]));
+      }
+      store_vec(dst + i0, x1[u]);
+      store_vec(dst + half + i0, x2[u]);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_typed(const QkvProblem& p, cudaStream_t stream) {
+  constexpr int VEC = 16 / sizeof(T);
+  QkvArgs a;
+  a.T = p.T;
+  a.B = p.B;
+  a.max_seq = p.max_seq;
+  a.nq = (int32_t)p.nq;
+  a.nk = (int32_t)p.nk;
+  a.nv = (int32_t)p.nv;
+  a.D = (int32_t)p.D;
+  a.W = (p.nq + p.nk + p.nv) * p.D;
+  a.block_size = (int32_t)p.block_size;
+  a.num_slots = p.num_blocks * p.block_size;
+  a.chunks = (int32_t)(p.D / 2 / VEC);
+  a.group = 1;
+  while (a.group < a.chunks) a.group *= 2;
+  a.head_chunks = (int32_t)((p.nq + p.nk + p.nv + kRowsInFlight - 1) / kRowsInFlight);
+  a.items = p.T * a.head_chunks;
+  a.eps = p.eps;
+  a.inv_d = 1.0f / (float)p.D;
+  const int64_t groups = kThreads / a.group;
+  auto kernel = qkv_kernel<T, VEC>;
+  const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), kThreads);
+  const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
+  unsigned int* err = nullptr;
+  const cudaError_t e = device_error_address(&err);
+  if (e != cudaSuccess) return e;
+  return launch_overlapped(kernel, (unsigned)grid, kThreads, stream, static_cast<const T*>(p.qkv),
+                           static_cast<const T*>(p.q_gamma), static_cast<const T*>(p.k_gamma),
+                           static_cast<const T*>(p.cache), p.seq_lens, p.query_start_loc, p.slot_mapping,
+                           static_cast<T*>(p.q_out), static_cast<T*>(p.k_cache), static_cast<T*>(p.v_cache), err,
+                           a);
+}
+
+}  // namespace
+
+cudaError_t launch_qkv(const QkvProblem& p, cudaStream_t stream) {
+  switch (p.dtype) {
+    case kF32:
+      return launch_typed<float>(p, stream);
+    case kF16:
+      return launch_typed<__half>(p, stream);
+    case kBF16:
+      return launch_typed<__nv_bfloat16>(p, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace rope
