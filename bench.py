@@ -53,7 +53,16 @@ def build_workloads():
 
 def algorithmic_bytes(case) -> int:
     """Read + write of rotated elements, cos/sin (or one gathered cache row per
-    token), positions.  Pass-through columns are never touched and not counted."""
+    token), positions.  Pass-through columns are never touched and not counted.
+    Fused QKV operator: read of qkv, write of q_out and of the cached K/V rows,
+    one gathered cache row per token, gammas and the int64 metadata."""
+    if hasattr(case, "qkv"):
+        e = case.qkv.element_size()
+        T, D = case.tokens, case.head_size
+        cached = int((case.slot_mapping >= 0).sum())
+        meta = (case.seq_lens.numel() + case.query_start_loc.numel() + case.slot_mapping.numel()) * 8
+        return (T * (case.nq + case.nk + case.nv) * D * e + T * case.nq * D * e + cached * (case.nk + case.nv) * D * e
+                + T * D * e + 2 * D * e + meta)
     if hasattr(case, "x"):
         B, S, N, D = case.x.shape
         L = D if (case.start, case.end) == (0, 0) else case.end - case.start
@@ -378,6 +387,15 @@ def time_next_rows(cases, dev_tensors, calls, steps):
     rows.append(("rope_gptj_fused_qkv_views_" + gptj.name.split("_", 2)[2], algorithmic_bytes(gptj),
                  R.prepare_with_sin_cos_cache(p4, qkv[:, :wq], qkv[:, wq:wq + wk], c4, hs, gptj.rotary_dim, False),
                  calls[1]))
+    # fused QKV split + RMSNorm + RoPE + paged cache write (mixed prefill/decode batch)
+    import workloads as W
+    qc = W.qkv_rmsnorm_rope_bf16()
+    dv = q3.device
+    qt = [t.to(dv) for t in (qc.qkv, qc.q_gamma, qc.k_gamma, qc.cache, qc.seq_lens, qc.query_start_loc,
+                             qc.slot_mapping, qc.q_out, qc.k_cache, qc.v_cache)]
+    rows.append((qc.name, algorithmic_bytes(qc),
+                 R.prepare_qkv_rmsnorm_rope_cache(qt[0], qc.nq, qc.nk, qc.nv, qt[1], qt[2], qc.eps, qt[3], qt[4],
+                                                  qt[5], qt[6], qt[7], qt[8], qt[9]), calls[3]))
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(rows))] for _ in range(steps)]
     for _ in range(3):
         for _, _, call, flush in rows:
