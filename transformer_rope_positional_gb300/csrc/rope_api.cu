@@ -36,19 +36,19 @@ int sm_count() {
   return g_sm_count[dev];
 }
 
-int resident_blocks(const void* kernel, int threads) {
+int resident_blocks(const void* kernel, int threads, size_t smem) {
   static std::mutex mu;
-  static std::map<std::tuple<int, const void*, int>, int> cache;
+  static std::map<std::tuple<int, const void*, int, size_t>, int> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
-  const auto key = std::make_tuple(dev, kernel, threads);
+  const auto key = std::make_tuple(dev, kernel, threads, smem);
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) {
     (void)cudaGetLastError();  // do not leave a sticky-looking error for the launch check
     n = 1;
   }

@@ -88,9 +88,10 @@ cudaError_t device_error_address(unsigned int** out);
 // Launch bookkeeping.
 void count_launch();
 int sm_count();
-// CTAs of `kernel` (launched with `threads` threads, no dynamic shared memory)
-// that fit on one SM of the current device; cached, at least 1.
-int resident_blocks(const void* kernel, int threads);
+// CTAs of `kernel` (launched with `threads` threads and `smem` bytes of
+// dynamic shared memory) that fit on one SM of the current device; cached, at
+// least 1.
+int resident_blocks(const void* kernel, int threads, size_t smem = 0);
 
 // Launch `kernel` on `stream` with programmatic stream serialization allowed:
 // the kernel may be scheduled while the previous kernel of the stream drains,
@@ -98,12 +99,12 @@ int resident_blocks(const void* kernel, int threads);
 // first global memory access, so stream order is unchanged; only the launch
 // latency is overlapped with the previous kernel's tail.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_overlapped(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t stream,
-                              Args... args) {
+cudaError_t launch_overlapped_smem(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                                   cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -113,6 +114,12 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), unsigned grid, unsigned 
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
   count_launch();
   return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t stream,
+                              Args... args) {
+  return launch_overlapped_smem(kernel, grid, block, 0, stream, args...);
 }
 
 }  // namespace rope

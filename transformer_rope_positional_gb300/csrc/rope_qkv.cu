@@ -17,7 +17,8 @@
 // (groups are padded to a power of two lanes), so a head never leaves
 // registers: one read of qkv, one write of q_out or of the cache slot.  The
 // per-token metadata (batch by binary search over queryStartLoc, position,
-// slot) is computed once per item.  Positions outside the table and slots past
+// slot) is computed once per item, searching a shared-memory copy of
+// queryStartLoc.  Positions outside the table and slots past
 // the pool set bits of the device error word and skip the writes.
 #include <algorithm>
 
@@ -37,6 +38,7 @@ constexpr int kRowsInFlight = ROPE_QKV_ROWS_IN_FLIGHT;
 constexpr int kThreads = ROPE_QKV_THREADS;
 constexpr unsigned kPositionOutOfRange = 1u;
 constexpr unsigned kSlotOutOfRange = 2u;
+constexpr int64_t kSharedQsl = 4096;  // queryStartLoc entries kept in shared memory (32 KB)
 
 struct QkvArgs {
   int64_t T, B;
@@ -73,12 +75,13 @@ __global__ void __launch_bounds__(kThreads)
   const int H = a.nq + a.nk + a.nv;
   wait_for_prior_grid();
 
-  // gamma of this thread's elements, both branches, both halves
-  Vec<T, VEC> gq1, gq2, gk1, gk2;
-  load_vec<false>(gq1, q_gamma + i0);
-  load_vec<false>(gq2, q_gamma + half + i0);
-  load_vec<false>(gk1, k_gamma + i0);
-  load_vec<false>(gk2, k_gamma + half + i0);
+  // queryStartLoc in shared memory for the batch lookup when it fits
+  extern __shared__ int64_t s_qsl[];
+  const bool qsl_shared = a.B + 1 <= kSharedQsl;
+  if (qsl_shared) {
+    for (int64_t i = threadIdx.x; i <= a.B; i += blockDim.x) s_qsl[i] = __ldg(qsl + i);
+    __syncthreads();
+  }
 
   for (int64_t item = (int64_t)blockIdx.x * P + g; item < a.items; item += (int64_t)gridDim.x * P) {
     const int64_t t = item / a.head_chunks;
@@ -97,9 +100,10 @@ __global__ void __launch_bounds__(kThreads)
     int64_t lo = 0, hi = a.B - 1;
     while (lo < hi) {
       const int64_t mid = (lo + hi + 1) / 2;
-      if (__ldg(qsl + mid) <= t) lo = mid; else hi = mid - 1;
+      if ((qsl_shared ? s_qsl[mid] : __ldg(qsl + mid)) <= t) lo = mid; else hi = mid - 1;
     }
-    const int64_t start = __ldg(qsl + lo), qlen = __ldg(qsl + lo + 1) - start;
+    const int64_t start = qsl_shared ? s_qsl[lo] : __ldg(qsl + lo);
+    const int64_t qlen = (qsl_shared ? s_qsl[lo + 1] : __ldg(qsl + lo + 1)) - start;
     const int64_t position = __ldg(seq_lens + lo) - qlen + (t - start);
     const int64_t slot = __ldg(slot_mapping + t);
     const bool pos_ok = position >= 0 && position < a.max_seq;
@@ -109,9 +113,9 @@ __global__ void __launch_bounds__(kThreads)
       else if (slot >= a.num_slots) atomicOr(err, kSlotOutOfRange);
     }
     if (!pos_ok) continue;  // nothing of this token is written
-    float cf[VEC], sf[VEC];
-    load_f32<T, VEC>(cf, cache + position * a.D + i0);
-    load_f32<T, VEC>(sf, cache + position * a.D + half + i0);
+    Vec<T, VEC> cv, sv;  // kept in the storage type; widened at each use
+    load_vec<false>(cv, cache + position * a.D + i0);
+    load_vec<false>(sv, cache + position * a.D + half + i0);
     const int64_t blk = cache_it ? slot / a.block_size : 0, off = cache_it ? slot % a.block_size : 0;
 
 #pragma unroll
@@ -143,14 +147,20 @@ __global__ void __launch_bounds__(kThreads)
       T* dst = is_q ? q_out + (t * a.nq + h) * (int64_t)a.D
                     : (cache_it ? k_cache + ((blk * a.nk + (h - a.nq)) * a.block_size + off) * a.D : nullptr);
       if (dst == nullptr) continue;
-      const Vec<T, VEC>& g1 = is_q ? gq1 : gk1;
-      const Vec<T, VEC>& g2 = is_q ? gq2 : gk2;
+      // gamma of this thread's elements (L1-resident, reloaded per row to save registers)
+      const T* gamma = is_q ? q_gamma : k_gamma;
+      Vec<T, VEC> g1, g2;
+      load_vec<false>(g1, gamma + i0);
+      load_vec<false>(g2, gamma + half + i0);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         const float y1 = __fmul_rn(__fmul_rn(widen(x1[u].e[e]), inv), widen(g1.e[e]));
         const float y2 = __fmul_rn(__fmul_rn(widen(x2[u].e[e]), inv), widen(g2.e[e]));
-        x1[u].e[e] = narrow<T>(diff_of_products(y1, cf[e], y2, sf[e]));
-        x2[u].e[e] = narrow<T>(diff_of_products(y2, cf[e], -y1, sf[e]));
+        const float c = widen(cv.e[e]), s = widen(sv.e[e]);
+        // y1, y2 already carry binary32 rounding from the normalisation, so a
+        // plain FMA pair is as accurate here as the compensated form
+        x1[u].e[e] = narrow<T>(__fmaf_rn(y1, c, -__fmul_rn(y2, s)));
+        x2[u].e[e] = narrow<T>(__fmaf_rn(y2, c, __fmul_rn(y1, s)));
       }
       store_vec(dst + i0, x1[u]);
       store_vec(dst + half + i0, x2[u]);
@@ -181,12 +191,15 @@ cudaError_t launch_typed(const QkvProblem& p, cudaStream_t stream) {
   a.inv_d = 1.0f / (float)p.D;
   const int64_t groups = kThreads / a.group;
   auto kernel = qkv_kernel<T, VEC>;
-  const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), kThreads);
+  // occupancy with the largest shared-memory request the kernel can make
+  const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), kThreads,
+                                                                 kSharedQsl * sizeof(int64_t));
   const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
   unsigned int* err = nullptr;
   const cudaError_t e = device_error_address(&err);
   if (e != cudaSuccess) return e;
-  return launch_overlapped(kernel, (unsigned)grid, kThreads, stream, static_cast<const T*>(p.qkv),
+  const size_t smem = p.B + 1 <= kSharedQsl ? (size_t)(p.B + 1) * sizeof(int64_t) : 0;
+  return launch_overlapped_smem(kernel, (unsigned)grid, kThreads, smem, stream, static_cast<const T*>(p.qkv),
                            static_cast<const T*>(p.q_gamma), static_cast<const T*>(p.k_gamma),
                            static_cast<const T*>(p.cache), p.seq_lens, p.query_start_loc, p.slot_mapping,
                            static_cast<T*>(p.q_out), static_cast<T*>(p.k_cache), static_cast<T*>(p.v_cache), err,
