@@ -292,8 +292,10 @@ def qkv_case(name: str, seed: int, query_lens: Sequence[int], context_lens: Sequ
              nv: int, head_size: int, block_size: int, dtype: torch.dtype, base: float = 10000.0,
              eps: float = 1e-6, pad_every: int = 0) -> QkvCase:
     """Batches with ``query_lens[b]`` new tokens on top of ``context_lens[b]``
-    cached ones (seqLens = context + query).  Every token gets a distinct cache
-    slot drawn at random from the pool (its KV blocks), except that with
+    cached ones (seqLens = context + query).  Paged cache as in paged-attention
+    serving: every sequence owns ceil(seqLen / block_size) blocks drawn from a
+    shuffled pool, and the token at position p goes to slot
+    block_table[p // block_size] * block_size + p % block_size.  With
     ``pad_every`` > 0 every pad_every-th token gets slot -1 (padding)."""
     T = int(sum(query_lens))
     seq_lens = torch.tensor([c + q for c, q in zip(context_lens, query_lens)], dtype=torch.int64)
@@ -305,9 +307,16 @@ def qkv_case(name: str, seed: int, query_lens: Sequence[int], context_lens: Sequ
     k_gamma = (1.0 + 0.25 * g[1]).to(dtype)
     max_seq = int(seq_lens.max()) + 1
     cache = cos_sin_cache(max_seq, head_size, base, dtype)
-    num_blocks = (T + block_size - 1) // block_size + 1
-    u = uniform(stream_seed(seed, 2), num_blocks * block_size)
-    slots = torch.from_numpy(np.argsort(u, kind="stable")[:T].astype(np.int64))
+    blocks_per_seq = [(int(n) + block_size - 1) // block_size for n in seq_lens]
+    num_blocks = sum(blocks_per_seq) + 1
+    pool = np.argsort(uniform(stream_seed(seed, 2), num_blocks), kind="stable")
+    slots = torch.empty(T, dtype=torch.int64)
+    first = 0
+    for b, (q_len, c_len) in enumerate(zip(query_lens, context_lens)):
+        table = pool[sum(blocks_per_seq[:b]):sum(blocks_per_seq[:b + 1])]
+        p = np.arange(c_len, c_len + q_len)
+        slots[first:first + q_len] = torch.from_numpy(table[p // block_size] * block_size + p % block_size)
+        first += q_len
     if pad_every:
         slots[::pad_every] = -1
     q_out = torch.full((T, nq * head_size), 3.0, dtype=dtype)
@@ -318,11 +327,11 @@ def qkv_case(name: str, seed: int, query_lens: Sequence[int], context_lens: Sequ
 
 
 def qkv_rmsnorm_rope_bf16() -> QkvCase:
-    """Mixed prefill/decode batch: 4 prefill chunks of 1920 tokens after 4096
-    cached ones, then 512 decode requests with 100..8000 cached tokens; 32 q,
-    8 k, 8 v heads of 128; bf16; 128-token KV blocks; seed 5."""
-    ctx_dec = (100 + uniform_int(stream_seed(5, 3), 512, 0, 7900)).tolist()
-    query_lens = [1920] * 4 + [1] * 512
+    """Mixed prefill/decode batch of 8192 new tokens: 4 prefill chunks of 1984
+    tokens after 4096 cached ones, then 256 decode requests with 16..1023 cached
+    tokens; 32 q, 8 k, 8 v heads of 128; bf16; 16-token KV blocks; seed 5."""
+    ctx_dec = uniform_int(stream_seed(5, 3), 256, 16, 1024).tolist()
+    query_lens = [1984] * 4 + [1] * 256
     context_lens = [4096] * 4 + ctx_dec
     return qkv_case("qkv_rmsnorm_rope_bf16_8192tok_32q8k8v_h128", 5, query_lens, context_lens, 32, 8, 8, 128,
-                    128, torch.bfloat16)
+                    16, torch.bfloat16)
