@@ -32,6 +32,33 @@ __device__ __forceinline__ __half narrow<__half>(float v) { return __float2half_
 template <>
 __device__ __forceinline__ __nv_bfloat16 narrow<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
+// Adjacent element pairs <-> float2, for the packed binary32 instructions
+// (__ffma2_rn, __fmul2_rn) that issue two lanes of arithmetic at once.
+__device__ __forceinline__ float2 widen2(const float* p) { return make_float2(p[0], p[1]); }
+__device__ __forceinline__ float2 widen2(const __half* p) {
+  return __half22float2(*reinterpret_cast<const __half2*>(p));
+}
+__device__ __forceinline__ float2 widen2(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ void narrow2(float* p, float2 v) {
+  p[0] = v.x;
+  p[1] = v.y;
+}
+__device__ __forceinline__ void narrow2(__half* p, float2 v) {
+  *reinterpret_cast<__half2*>(p) = __floats2half2_rn(v.x, v.y);
+}
+__device__ __forceinline__ void narrow2(__nv_bfloat16* p, float2 v) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
+}
+
+// Quotient of a non-negative index by a positive divisor, in 32-bit
+// arithmetic when the host has checked that both fit (much cheaper than the
+// 64-bit division sequence).
+__device__ __forceinline__ int64_t div_index(int64_t n, int64_t d, bool fits32) {
+  return fits32 ? (int64_t)((uint32_t)n / (uint32_t)d) : n / d;
+}
+
 // ---------------------------------------------------------------------------
 // a*b - c*d with relative error at most 2^-23 (Kahan's algorithm: the rounding
 // error of c*d is recovered exactly by an FMA and added back; bound from

@@ -54,6 +54,7 @@ struct QkvArgs {
   int32_t head_chunks;  // ceil(H / U)
   float eps;
   float inv_d;
+  bool items32;  // items and slots fit 32-bit index arithmetic
 };
 
 template <typename T, int VEC>
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   for (int64_t item = (int64_t)blockIdx.x * P + g; item < a.items; item += (int64_t)gridDim.x * P) {
-    const int64_t t = item / a.head_chunks;
+    const int64_t t = div_index(item, a.head_chunks, a.items32);
     const int h0 = (int)(item - t * a.head_chunks) * U;
     const int n = min(U, H - h0);
     // ---- issue the loads of the item's head rows
@@ -116,51 +117,63 @@ __global__ void __launch_bounds__(kThreads)
     Vec<T, VEC> cv, sv;  // kept in the storage type; widened at each use
     load_vec<false>(cv, cache + position * a.D + i0);
     load_vec<false>(sv, cache + position * a.D + half + i0);
-    const int64_t blk = cache_it ? slot / a.block_size : 0, off = cache_it ? slot % a.block_size : 0;
+    const int64_t blk = cache_it ? div_index(slot, a.block_size, a.items32) : 0;
+    const int64_t off = cache_it ? slot - blk * a.block_size : 0;
+
+    // ---- RMSNorm: squares of every q/k row of the item (independent chains),
+    // then butterflies inside the row group, interleaved across the rows
+    float ss[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float2 acc = make_float2(0.f, 0.f);
+      if (u < n && h0 + u < a.nq + a.nk && active) {
+#pragma unroll
+        for (int j = 0; j < VEC; j += 2) {
+          const float2 v1 = widen2(&x1[u].e[j]), v2 = widen2(&x2[u].e[j]);
+          acc = __ffma2_rn(v1, v1, acc);
+          acc = __ffma2_rn(v2, v2, acc);
+        }
+      }
+      ss[u] = acc.x + acc.y;
+    }
+    for (int m = G / 2; m > 0; m /= 2)
+#pragma unroll
+      for (int u = 0; u < U; ++u) ss[u] += __shfl_xor_sync(gmask, ss[u], m, G);
+    if (!active) continue;
 
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (u >= n) break;
       const int h = h0 + u;
       if (h >= a.nq + a.nk) {  // V: stored as is
-        if (cache_it && active) {
+        if (cache_it) {
           T* dst = v_cache + ((blk * a.nv + (h - a.nq - a.nk)) * a.block_size + off) * a.D;
           store_vec(dst + i0, x1[u]);
           store_vec(dst + half + i0, x2[u]);
         }
         continue;
       }
-      // RMSNorm: this thread's squares, then a butterfly inside the row group
-      float ss = 0.f;
-      if (active) {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const float v1 = widen(x1[u].e[e]), v2 = widen(x2[u].e[e]);
-          ss = __fmaf_rn(v1, v1, ss);
-          ss = __fmaf_rn(v2, v2, ss);
-        }
-      }
-      for (int m = G / 2; m > 0; m /= 2) ss += __shfl_xor_sync(gmask, ss, m, G);
-      const float inv = rsqrtf(__fmaf_rn(ss, a.inv_d, a.eps));
-      if (!active) continue;
       const bool is_q = h < a.nq;
       T* dst = is_q ? q_out + (t * a.nq + h) * (int64_t)a.D
                     : (cache_it ? k_cache + ((blk * a.nk + (h - a.nq)) * a.block_size + off) * a.D : nullptr);
       if (dst == nullptr) continue;
+      const float inv = rsqrtf(__fmaf_rn(ss[u], a.inv_d, a.eps));
+      const float2 inv2 = make_float2(inv, inv);
       // gamma of this thread's elements (L1-resident, reloaded per row to save registers)
       const T* gamma = is_q ? q_gamma : k_gamma;
       Vec<T, VEC> g1, g2;
       load_vec<false>(g1, gamma + i0);
       load_vec<false>(g2, gamma + half + i0);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const float y1 = __fmul_rn(__fmul_rn(widen(x1[u].e[e]), inv), widen(g1.e[e]));
-        const float y2 = __fmul_rn(__fmul_rn(widen(x2[u].e[e]), inv), widen(g2.e[e]));
-        const float c = widen(cv.e[e]), s = widen(sv.e[e]);
+      for (int j = 0; j < VEC; j += 2) {
+        const float2 y1 = __fmul2_rn(__fmul2_rn(widen2(&x1[u].e[j]), inv2), widen2(&g1.e[j]));
+        const float2 y2 = __fmul2_rn(__fmul2_rn(widen2(&x2[u].e[j]), inv2), widen2(&g2.e[j]));
+        const float2 cs = widen2(&cv.e[j]), sn = widen2(&sv.e[j]);
         // y1, y2 already carry binary32 rounding from the normalisation, so a
         // plain FMA pair is as accurate here as the compensated form
-        x1[u].e[e] = narrow<T>(__fmaf_rn(y1, c, -__fmul_rn(y2, s)));
-        x2[u].e[e] = narrow<T>(__fmaf_rn(y2, c, __fmul_rn(y1, s)));
+        const float2 t2 = __fmul2_rn(y2, sn), t1 = __fmul2_rn(y1, sn);
+        narrow2(&x1[u].e[j], __ffma2_rn(y1, cs, make_float2(-t2.x, -t2.y)));
+        narrow2(&x2[u].e[j], __ffma2_rn(y2, cs, t1));
       }
       store_vec(dst + i0, x1[u]);
       store_vec(dst + half + i0, x2[u]);
@@ -189,6 +202,7 @@ cudaError_t launch_typed(const QkvProblem& p, cudaStream_t stream) {
   a.items = p.T * a.head_chunks;
   a.eps = p.eps;
   a.inv_d = 1.0f / (float)p.D;
+  a.items32 = a.items <= 0xffffffffLL && a.num_slots <= 0xffffffffLL;
   const int64_t groups = kThreads / a.group;
   auto kernel = qkv_kernel<T, VEC>;
   // occupancy with the largest shared-memory request the kernel can make
