@@ -562,6 +562,59 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_marginal(args):
+    """Each hot-path kernel alone, at its token count and at twice that, with a
+    read-only sweep of 384 MB before every launch (clean, cold L2).  Reports the
+    clean single-launch GB/s, the marginal GB/s (extra bytes / extra time) and
+    the fixed cost (launch, ramp-up, drain) that separates the two."""
+    import workloads as W
+    from transformer_rope_positional_gb300 import build as B
+    B.build()
+    import transformer_rope_positional_gb300 as R
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sweep = torch.empty(384 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def prep(c):
+        if hasattr(c, "x"):
+            return R.prepare_inplace_partial(c.x.to(dev), c.cos.to(dev), c.sin.to(dev), 1, [c.start, c.end])
+        return R.prepare_with_sin_cos_cache(c.positions.to(dev), c.query.to(dev), c.key.to(dev), c.cache.to(dev),
+                                            c.head_size, c.rotary_dim, c.is_neox, c.mrope_section)
+
+    def median_us(call, reps=30):
+        ts = []
+        for _ in range(3):
+            call()
+        for _ in range(reps):
+            sink.copy_(sweep.sum().reshape(1))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return sorted(ts)[len(ts) // 2] * 1e3
+
+    mrope = W.mrope_neox_bf16()
+    pairs = [(W.inplace_bf16_mixed(4), W.inplace_bf16_mixed(8)),
+             (W.cache_neox_bf16(16384), W.cache_neox_bf16(32768)),
+             (W.cache_gptj_f16_partial(8, 1024), W.cache_gptj_f16_partial(16, 1024)),
+             (mrope, W.cache_case(mrope.name + "_x2", 4, 2 * mrope.tokens, 28, 4, 128, 128, 40960, torch.bfloat16,
+                                  True, base=1e6, positions=torch.cat([mrope.positions] * 2, 1).contiguous(),
+                                  mrope_section=[16, 24, 24]))]
+    peak, _ = measured_peak()
+    out = []
+    for c1, c2 in pairs:
+        t1, t2 = median_us(prep(c1)), median_us(prep(c2))
+        b1, b2 = algorithmic_bytes(c1), algorithmic_bytes(c2)
+        marg = (b2 - b1) / ((t2 - t1) * 1e-6) / 1e9
+        out.append({"workload": c1.name, "us_1x": round(t1, 2), "us_2x": round(t2, 2),
+                    "gbs_1x": round(b1 / (t1 * 1e-6) / 1e9, 1), "frac_1x": round(b1 / (t1 * 1e-6) / 1e9 / peak, 4),
+                    "marginal_gbs": round(marg, 1), "fixed_us": round(t1 - b1 / (marg * 1e9) * 1e6, 2)})
+    print(json.dumps({"mode": "marginal", "peak_gbs": peak, "kernels": out}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -573,11 +626,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle work for cpu_baseline")
     ap.add_argument("--reference-seconds", type=float, default=120.0, help="oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--marginal", action="store_true",
+                    help="instead of the step: each kernel alone at 1x and 2x tokens on a clean L2")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.marginal:
+        run_marginal(args)
     else:
         run_ours(args)
 
