@@ -9,17 +9,29 @@
 //   q_out[t, h] = y_rope;  kCache[slot/BS, h, slot%BS] = y_rope;  vCache[...] = v
 // cos/sin are the halves of row `position` of a [maxSeq, D] cos||sin table.
 //
-// GB300 design.  Same streaming structure as the other kernels: items of U
-// consecutive heads of one token, row groups of C threads (thread c owns the
-// c-th 16-byte chunk of both halves of a head, the NeoX pairing), persistent
-// grid striding over items.  The RMSNorm reduction is a sum of the thread's
-// 2*VEC squares followed by a butterfly of warp shuffles inside the row group
-// (groups are padded to a power of two lanes), so a head never leaves
-// registers: one read of qkv, one write of q_out or of the cache slot.  The
-// per-token metadata (batch by binary search over queryStartLoc, position,
-// slot) is computed once per item, searching a shared-memory copy of
-// queryStartLoc.  Positions outside the table and slots past
-// the pool set bits of the device error word and skip the writes.
+// GB300 design.  Same streaming structure as the other kernels: items of up
+// to U consecutive heads of one token, row groups of C threads (thread c owns
+// the c-th 16-byte chunk of both halves of a head, the NeoX pairing),
+// persistent grid striding over items.  Items never mix q, k and v heads (a
+// token has ceil(Nq/U) q items, then ceil(Nk/U) k items, then ceil(Nv/U) v
+// items), so one item has one gamma and one destination layout.
+//
+//  * RMSNorm: each thread sums the squares of its 2*VEC elements, then a
+//    butterfly of warp shuffles inside the row group (padded to a power of two
+//    lanes) completes the head's sum; a head never leaves registers.
+//  * RoPE with the norm folded in: per item, thread c forms the products
+//    gamma_low*cos, -gamma_high*sin, gamma_high*cos, gamma_low*sin of its
+//    elements once, so each output element costs one product, one FMA and
+//    the scaling by 1/rms:  out_low = (x_low*(g_low*cos) - x_high*(g_high*sin)) / rms.
+//  * Token metadata (batch by search in queryStartLoc, position, slot) for
+//    the NEXT item is computed while the current item's loads are in flight,
+//    so the search and the dependent loads leave the critical path.  With few
+//    enough sequences, queryStartLoc and seqLens[b] - queryStartLoc[b+1] sit in
+//    shared memory (position = t + that difference), and the search starts
+//    from the previous item's batch (a group's tokens only increase).
+//
+// Positions outside the table and slots past the pool set bits of the device
+// error word and skip the writes.
 #include <algorithm>
 
 #include "rope_device.cuh"
@@ -34,31 +46,79 @@ namespace {
 #ifndef ROPE_QKV_THREADS
 #define ROPE_QKV_THREADS 128
 #endif
+// 4 CTAs per SM caps the kernel at 128 registers per thread without spills;
+// measured faster than both the uncapped build (3 CTAs) and 5 CTAs with spills.
+#ifndef ROPE_QKV_MIN_BLOCKS
+#define ROPE_QKV_MIN_BLOCKS 4
+#endif
 constexpr int kRowsInFlight = ROPE_QKV_ROWS_IN_FLIGHT;
 constexpr int kThreads = ROPE_QKV_THREADS;
 constexpr unsigned kPositionOutOfRange = 1u;
 constexpr unsigned kSlotOutOfRange = 2u;
-constexpr int64_t kSharedQsl = 4096;  // queryStartLoc entries kept in shared memory (32 KB)
+constexpr int64_t kSharedTable = 4096;  // int64 entries of the shared batch tables (32 KB)
 
 struct QkvArgs {
   int64_t T, B;
   int64_t max_seq;
   int64_t W;          // qkv row width, (nq + nk + nv) * D
   int64_t num_slots;  // num_blocks * block_size
-  int64_t items;      // T * head_chunks
+  int64_t items;      // T * per_token
   int32_t nq, nk, nv;
+  int32_t iq, ik;       // q items and k items per token
+  int32_t per_token;    // items per token, iq + ik + ceil(nv / U)
   int32_t D;
   int32_t block_size;
   int32_t chunks;       // C: active threads per head row
   int32_t group;        // C rounded up to a power of two (lanes per row group)
-  int32_t head_chunks;  // ceil(H / U)
   float eps;
   float inv_d;
   bool items32;  // items and slots fit 32-bit index arithmetic
 };
 
-template <typename T, int VEC>
-__global__ void __launch_bounds__(kThreads)
+// Token metadata of one item.
+struct ItemMeta {
+  int64_t t;         // token
+  int64_t position;  // row of the cos/sin table
+  int64_t slot;      // slot_mapping[t]
+  int32_t r;         // item index within the token
+  int32_t b;         // batch of the token
+};
+
+// Batch of token t: the largest b in [0, B) with queryStartLoc[b] <= t.  `lo`
+// is a batch with queryStartLoc[lo] <= t (the previous answer for a smaller
+// or equal token, or 0): the common case is one comparison.
+__device__ __forceinline__ int find_batch(const int64_t* __restrict__ qsl, int B, int64_t t, int lo) {
+  if (lo + 1 < B && qsl[lo + 1] <= t) {
+    int l = lo + 1, h = B - 1;
+    while (l < h) {
+      const int mid = (l + h + 1) >> 1;
+      if (qsl[mid] <= t) l = mid; else h = mid - 1;
+    }
+    lo = l;
+  }
+  return lo;
+}
+
+template <bool SHARED>
+__device__ __forceinline__ ItemMeta item_meta(int64_t item, const QkvArgs& a, const int64_t* __restrict__ tab,
+                                              const int64_t* __restrict__ qsl, const int64_t* __restrict__ seq_lens,
+                                              const int64_t* __restrict__ slot_mapping, int cursor) {
+  ItemMeta m;
+  m.t = div_index(item, a.per_token, a.items32);
+  m.r = (int32_t)(item - m.t * a.per_token);
+  m.slot = __ldg(slot_mapping + m.t);
+  if (SHARED) {
+    m.b = find_batch(tab, (int)a.B, m.t, cursor);
+    m.position = m.t + tab[a.B + 1 + m.b];
+  } else {
+    m.b = find_batch(qsl, (int)a.B, m.t, cursor);
+    m.position = __ldg(seq_lens + m.b) - __ldg(qsl + m.b + 1) + m.t;
+  }
+  return m;
+}
+
+template <typename T, int VEC, bool SHARED>
+__global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
     qkv_kernel(const T* __restrict__ qkv, const T* __restrict__ q_gamma, const T* __restrict__ k_gamma,
                const T* __restrict__ cache, const int64_t* __restrict__ seq_lens, const int64_t* __restrict__ qsl,
                const int64_t* __restrict__ slot_mapping, T* __restrict__ q_out, T* __restrict__ k_cache,
@@ -73,117 +133,164 @@ __global__ void __launch_bounds__(kThreads)
   const unsigned gmask = (G >= 32 ? 0xffffffffu : ((1u << G) - 1u)) << (lane & ~(G - 1));
   const int half = a.D / 2;
   const int i0 = (active ? c : 0) * VEC;
-  const int H = a.nq + a.nk + a.nv;
   wait_for_prior_grid();
 
-  // queryStartLoc in shared memory for the batch lookup when it fits
-  extern __shared__ int64_t s_qsl[];
-  const bool qsl_shared = a.B + 1 <= kSharedQsl;
-  if (qsl_shared) {
-    for (int64_t i = threadIdx.x; i <= a.B; i += blockDim.x) s_qsl[i] = __ldg(qsl + i);
+  // [0, B]: queryStartLoc; [B + 1, 2B]: seqLens[b] - queryStartLoc[b + 1]
+  extern __shared__ int64_t s_tab[];
+  if (SHARED) {
+    for (int64_t i = threadIdx.x; i <= a.B; i += blockDim.x) s_tab[i] = __ldg(qsl + i);
+    for (int64_t i = threadIdx.x; i < a.B; i += blockDim.x)
+      s_tab[a.B + 1 + i] = __ldg(seq_lens + i) - __ldg(qsl + i + 1);
     __syncthreads();
   }
 
-  for (int64_t item = (int64_t)blockIdx.x * P + g; item < a.items; item += (int64_t)gridDim.x * P) {
-    const int64_t t = div_index(item, a.head_chunks, a.items32);
-    const int h0 = (int)(item - t * a.head_chunks) * U;
-    const int n = min(U, H - h0);
-    // ---- issue the loads of the item's head rows
+  const int64_t stride = (int64_t)gridDim.x * P;
+  int64_t item = (int64_t)blockIdx.x * P + g;
+  if (item >= a.items) return;
+  ItemMeta m = item_meta<SHARED>(item, a, s_tab, qsl, seq_lens, slot_mapping, 0);
+  for (; item < a.items; item += stride) {
+    // ---- this item's heads: kind 0 q, 1 k, 2 v; h0 within the kind
+    int kind, h0, nh, hg;
+    if (m.r < a.iq) {
+      kind = 0, h0 = m.r * U, nh = a.nq, hg = h0;
+    } else if (m.r < a.iq + a.ik) {
+      kind = 1, h0 = (m.r - a.iq) * U, nh = a.nk, hg = a.nq + h0;
+    } else {
+      kind = 2, h0 = (m.r - a.iq - a.ik) * U, nh = a.nv, hg = a.nq + a.nk + h0;
+    }
+    const int n = min(U, nh - h0);
+    const bool pos_ok = m.position >= 0 && m.position < a.max_seq;
+    const bool cache_it = m.slot >= 0 && m.slot < a.num_slots;
+    const bool work = pos_ok && (kind == 0 || cache_it);  // uniform over the row group
+    const bool rotate = kind < 2;
+    // ---- issue the loads: head rows, then cos/sin and gamma
     Vec<T, VEC> x1[U], x2[U];
-    const T* src = qkv + t * a.W + (int64_t)h0 * a.D;
+    Vec<T, VEC> cv, sv, g1, g2;
+    if (work && active) {
+      const T* src = qkv + m.t * a.W + (int64_t)hg * a.D + i0;
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (u < n && active) {
-        load_vec<true>(x1[u], src + u * a.D + i0);
-        load_vec<true>(x2[u], src + u * a.D + half + i0);
+      for (int u = 0; u < U; ++u)
+        if (u < n) {
+          load_vec<true>(x1[u], src + u * a.D);
+          load_vec<true>(x2[u], src + u * a.D + half);
+        }
+      if (rotate) {
+        const T* cs = cache + m.position * a.D + i0;
+        load_vec<false>(cv, cs);
+        load_vec<false>(sv, cs + half);
+        const T* gamma = (kind == 0 ? q_gamma : k_gamma) + i0;
+        load_vec<false>(g1, gamma);
+        load_vec<false>(g2, gamma + half);
       }
-    // ---- token metadata: batch (largest b with qsl[b] <= t), position, slot
-    int64_t lo = 0, hi = a.B - 1;
-    while (lo < hi) {
-      const int64_t mid = (lo + hi + 1) / 2;
-      if ((qsl_shared ? s_qsl[mid] : __ldg(qsl + mid)) <= t) lo = mid; else hi = mid - 1;
     }
-    const int64_t start = qsl_shared ? s_qsl[lo] : __ldg(qsl + lo);
-    const int64_t qlen = (qsl_shared ? s_qsl[lo + 1] : __ldg(qsl + lo + 1)) - start;
-    const int64_t position = __ldg(seq_lens + lo) - qlen + (t - start);
-    const int64_t slot = __ldg(slot_mapping + t);
-    const bool pos_ok = position >= 0 && position < a.max_seq;
-    const bool cache_it = slot >= 0 && slot < a.num_slots;
-    if (c == 0 && h0 == 0) {  // reported once per token
+    if (c == 0 && m.r == 0) {  // reported once per token
       if (!pos_ok) atomicOr(err, kPositionOutOfRange);
-      else if (slot >= a.num_slots) atomicOr(err, kSlotOutOfRange);
+      else if (m.slot >= a.num_slots) atomicOr(err, kSlotOutOfRange);
     }
-    if (!pos_ok) continue;  // nothing of this token is written
-    Vec<T, VEC> cv, sv;  // kept in the storage type; widened at each use
-    load_vec<false>(cv, cache + position * a.D + i0);
-    load_vec<false>(sv, cache + position * a.D + half + i0);
-    const int64_t blk = cache_it ? div_index(slot, a.block_size, a.items32) : 0;
-    const int64_t off = cache_it ? slot - blk * a.block_size : 0;
+    // destination of head h0 and the distance between consecutive heads
+    T* dst = nullptr;
+    int64_t dstride = a.D;
+    if (kind == 0) {
+      dst = q_out + (m.t * a.nq + h0) * (int64_t)a.D;
+    } else if (cache_it) {
+      const int64_t blk = div_index(m.slot, a.block_size, a.items32);
+      const int64_t off = m.slot - blk * a.block_size;
+      dst = (kind == 1 ? k_cache + ((blk * a.nk + h0) * a.block_size + off) * a.D
+                       : v_cache + ((blk * a.nv + h0) * a.block_size + off) * a.D);
+      dstride = (int64_t)a.block_size * a.D;
+    }
+    // ---- next item's metadata while the loads are in flight
+    const int64_t next = item + stride;
+    const ItemMeta mn = next < a.items ? item_meta<SHARED>(next, a, s_tab, qsl, seq_lens, slot_mapping, m.b) : m;
 
-    // ---- RMSNorm: squares of every q/k row of the item (independent chains),
-    // then butterflies inside the row group, interleaved across the rows
-    float ss[U];
+    if (work && rotate) {
+      // RMSNorm: squares of every row of the item (independent chains), then
+      // butterflies inside the row group, interleaved across the rows
+      float ss[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float2 acc = make_float2(0.f, 0.f);
-      if (u < n && h0 + u < a.nq + a.nk && active) {
+      for (int u = 0; u < U; ++u) {
+        float2 acc = make_float2(0.f, 0.f);
+        if (u < n && active) {
+#pragma unroll
+          for (int j = 0; j < VEC; j += 2) {
+            const float2 v1 = widen2(&x1[u].e[j]), v2 = widen2(&x2[u].e[j]);
+            acc = __ffma2_rn(v1, v1, acc);
+            acc = __ffma2_rn(v2, v2, acc);
+          }
+        }
+        ss[u] = acc.x + acc.y;
+      }
+      for (int sh = G / 2; sh > 0; sh /= 2)
+#pragma unroll
+        for (int u = 0; u < U; ++u) ss[u] += __shfl_xor_sync(gmask, ss[u], sh, G);
+      if (active) {
+        // gamma folded into cos/sin: ca = g_low*cos, cb = -g_high*sin,
+        // cc = g_high*cos, cd = g_low*sin
+        float2 ca[VEC / 2], cb[VEC / 2], cc[VEC / 2], cd[VEC / 2];
 #pragma unroll
         for (int j = 0; j < VEC; j += 2) {
-          const float2 v1 = widen2(&x1[u].e[j]), v2 = widen2(&x2[u].e[j]);
-          acc = __ffma2_rn(v1, v1, acc);
-          acc = __ffma2_rn(v2, v2, acc);
+          const float2 gl = widen2(&g1.e[j]), gh = widen2(&g2.e[j]);
+          const float2 co = widen2(&cv.e[j]), si = widen2(&sv.e[j]);
+          ca[j / 2] = __fmul2_rn(gl, co);
+          cb[j / 2] = __fmul2_rn(gh, make_float2(-si.x, -si.y));
+          cc[j / 2] = __fmul2_rn(gh, co);
+          cd[j / 2] = __fmul2_rn(gl, si);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (u >= n) break;
+          const float inv = rsqrtf(__fmaf_rn(ss[u], a.inv_d, a.eps));
+          const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+          for (int j = 0; j < VEC; j += 2) {
+            const float2 xl = widen2(&x1[u].e[j]), xh = widen2(&x2[u].e[j]);
+            // each product carries one binary32 rounding relative to the
+            // normalised terms, so a plain product + FMA is as accurate here
+            // as a compensated difference
+            const float2 lo = __ffma2_rn(xl, ca[j / 2], __fmul2_rn(xh, cb[j / 2]));
+            const float2 hi = __ffma2_rn(xh, cc[j / 2], __fmul2_rn(xl, cd[j / 2]));
+            narrow2(&x1[u].e[j], __fmul2_rn(lo, inv2));
+            narrow2(&x2[u].e[j], __fmul2_rn(hi, inv2));
+          }
+          store_vec(dst + u * dstride + i0, x1[u]);
+          store_vec(dst + u * dstride + half + i0, x2[u]);
         }
       }
-      ss[u] = acc.x + acc.y;
-    }
-    for (int m = G / 2; m > 0; m /= 2)
+    } else if (work && active) {  // V: stored as is
 #pragma unroll
-      for (int u = 0; u < U; ++u) ss[u] += __shfl_xor_sync(gmask, ss[u], m, G);
-    if (!active) continue;
-
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (u >= n) break;
-      const int h = h0 + u;
-      if (h >= a.nq + a.nk) {  // V: stored as is
-        if (cache_it) {
-          T* dst = v_cache + ((blk * a.nv + (h - a.nq - a.nk)) * a.block_size + off) * a.D;
-          store_vec(dst + i0, x1[u]);
-          store_vec(dst + half + i0, x2[u]);
+      for (int u = 0; u < U; ++u)
+        if (u < n) {
+          store_vec(dst + u * dstride + i0, x1[u]);
+          store_vec(dst + u * dstride + half + i0, x2[u]);
         }
-        continue;
-      }
-      const bool is_q = h < a.nq;
-      T* dst = is_q ? q_out + (t * a.nq + h) * (int64_t)a.D
-                    : (cache_it ? k_cache + ((blk * a.nk + (h - a.nq)) * a.block_size + off) * a.D : nullptr);
-      if (dst == nullptr) continue;
-      const float inv = rsqrtf(__fmaf_rn(ss[u], a.inv_d, a.eps));
-      const float2 inv2 = make_float2(inv, inv);
-      // gamma of this thread's elements (L1-resident, reloaded per row to save registers)
-      const T* gamma = is_q ? q_gamma : k_gamma;
-      Vec<T, VEC> g1, g2;
-      load_vec<false>(g1, gamma + i0);
-      load_vec<false>(g2, gamma + half + i0);
-#pragma unroll
-      for (int j = 0; j < VEC; j += 2) {
-        const float2 y1 = __fmul2_rn(__fmul2_rn(widen2(&x1[u].e[j]), inv2), widen2(&g1.e[j]));
-        const float2 y2 = __fmul2_rn(__fmul2_rn(widen2(&x2[u].e[j]), inv2), widen2(&g2.e[j]));
-        const float2 cs = widen2(&cv.e[j]), sn = widen2(&sv.e[j]);
-        // y1, y2 already carry binary32 rounding from the normalisation, so a
-        // plain FMA pair is as accurate here as the compensated form
-        const float2 t2 = __fmul2_rn(y2, sn), t1 = __fmul2_rn(y1, sn);
-        narrow2(&x1[u].e[j], __ffma2_rn(y1, cs, make_float2(-t2.x, -t2.y)));
-        narrow2(&x2[u].e[j], __ffma2_rn(y2, cs, t1));
-      }
-      store_vec(dst + i0, x1[u]);
-      store_vec(dst + half + i0, x2[u]);
     }
+    m = mn;
   }
+}
+
+template <typename T, bool SHARED>
+cudaError_t launch_tables(const QkvProblem& p, const QkvArgs& a, cudaStream_t stream) {
+  constexpr int VEC = 16 / sizeof(T);
+  const int64_t groups = kThreads / a.group;
+  auto kernel = qkv_kernel<T, VEC, SHARED>;
+  // shared tables rounded up to 4 KB so that few distinct sizes reach the occupancy cache
+  const size_t smem = SHARED ? (size_t)((2 * p.B + 1) * sizeof(int64_t) + 4095) / 4096 * 4096 : 0;
+  const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), kThreads, smem);
+  const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
+  unsigned int* err = nullptr;
+  const cudaError_t e = device_error_address(&err);
+  if (e != cudaSuccess) return e;
+  return launch_overlapped_smem(kernel, (unsigned)grid, kThreads, smem, stream, static_cast<const T*>(p.qkv),
+                                static_cast<const T*>(p.q_gamma), static_cast<const T*>(p.k_gamma),
+                                static_cast<const T*>(p.cache), p.seq_lens, p.query_start_loc, p.slot_mapping,
+                                static_cast<T*>(p.q_out), static_cast<T*>(p.k_cache), static_cast<T*>(p.v_cache),
+                                err, a);
 }
 
 template <typename T>
 cudaError_t launch_typed(const QkvProblem& p, cudaStream_t stream) {
   constexpr int VEC = 16 / sizeof(T);
+  constexpr int U = kRowsInFlight;
   QkvArgs a;
   a.T = p.T;
   a.B = p.B;
@@ -191,6 +298,9 @@ cudaError_t launch_typed(const QkvProblem& p, cudaStream_t stream) {
   a.nq = (int32_t)p.nq;
   a.nk = (int32_t)p.nk;
   a.nv = (int32_t)p.nv;
+  a.iq = (int32_t)((p.nq + U - 1) / U);
+  a.ik = (int32_t)((p.nk + U - 1) / U);
+  a.per_token = a.iq + a.ik + (int32_t)((p.nv + U - 1) / U);
   a.D = (int32_t)p.D;
   a.W = (p.nq + p.nk + p.nv) * p.D;
   a.block_size = (int32_t)p.block_size;
@@ -198,26 +308,12 @@ cudaError_t launch_typed(const QkvProblem& p, cudaStream_t stream) {
   a.chunks = (int32_t)(p.D / 2 / VEC);
   a.group = 1;
   while (a.group < a.chunks) a.group *= 2;
-  a.head_chunks = (int32_t)((p.nq + p.nk + p.nv + kRowsInFlight - 1) / kRowsInFlight);
-  a.items = p.T * a.head_chunks;
+  a.items = p.T * a.per_token;
   a.eps = p.eps;
   a.inv_d = 1.0f / (float)p.D;
   a.items32 = a.items <= 0xffffffffLL && a.num_slots <= 0xffffffffLL;
-  const int64_t groups = kThreads / a.group;
-  auto kernel = qkv_kernel<T, VEC>;
-  // occupancy with the largest shared-memory request the kernel can make
-  const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), kThreads,
-                                                                 kSharedQsl * sizeof(int64_t));
-  const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
-  unsigned int* err = nullptr;
-  const cudaError_t e = device_error_address(&err);
-  if (e != cudaSuccess) return e;
-  const size_t smem = p.B + 1 <= kSharedQsl ? (size_t)(p.B + 1) * sizeof(int64_t) : 0;
-  return launch_overlapped_smem(kernel, (unsigned)grid, kThreads, smem, stream, static_cast<const T*>(p.qkv),
-                           static_cast<const T*>(p.q_gamma), static_cast<const T*>(p.k_gamma),
-                           static_cast<const T*>(p.cache), p.seq_lens, p.query_start_loc, p.slot_mapping,
-                           static_cast<T*>(p.q_out), static_cast<T*>(p.k_cache), static_cast<T*>(p.v_cache), err,
-                           a);
+  if (2 * p.B + 1 <= kSharedTable) return launch_tables<T, true>(p, a, stream);
+  return launch_tables<T, false>(p, a, stream);
 }
 
 }  // namespace
