@@ -63,6 +63,7 @@ struct CacheArgs {
   int32_t section_end[4];
   int32_t cache_mode;      // 0 sectioned splice, 1 interleaved splice (V2)
   int32_t interleave_end;  // cache_mode 1: indices below 3 * mropeSection[1] interleave
+  bool items32;            // items fit 32-bit index arithmetic
 };
 
 // Section holding cos index i.  section_end[] holds cumulative ends and the
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
 
   // item = (token t, head chunk j): heads [j*U, min(j*U + U, heads)) of token t
   for (int64_t item = (int64_t)blockIdx.x * P + g; item < a.items; item += (int64_t)gridDim.x * P) {
-    const int64_t t = item / a.head_chunks;
+    const int64_t t = div_index(item, a.head_chunks, a.items32);
     const int h0 = (int)(item - t * a.head_chunks) * U;
     const int n = min(U, heads - h0);
     // ---- issue the loads of the chunk's rows
@@ -247,6 +248,7 @@ cudaError_t launch_typed(const CacheProblem& p, cudaStream_t stream) {
   a.interleave_end = p.cache_mode == 1 ? 3 * (p.section_end[1] - p.section_end[0]) : 0;
   a.head_chunks = (int32_t)((p.hq + p.hk + kRowsInFlight - 1) / kRowsInFlight);
   a.items = p.T * a.head_chunks;
+  a.items32 = a.items <= 0xffffffffLL;
   const int threads = kThreads;
   const int64_t groups = threads / a.chunks;
   // Persistent grid: the CTAs that fit on the GPU at once stride over the items,

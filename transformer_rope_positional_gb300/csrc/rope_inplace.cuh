@@ -64,6 +64,7 @@ struct InplaceArgs {
   int64_t items;        // B * S * head_chunks
   int32_t head_chunks;  // ceil(N / U): chunks of U consecutive heads per token
   int32_t chunks;       // threads per row
+  bool items32;         // items (and so tokens) fit 32-bit index arithmetic
 };
 
 // One pair (a at slot j, b at its partner j') with element-wise cos/sin.
@@ -123,11 +124,11 @@ __global__ void __launch_bounds__(512, ROPE_INPLACE_MIN_BLOCKS)
 
   // item = (token t, head chunk j): heads [j*U, min(j*U + U, N)) of token t
   for (int64_t item = (int64_t)blockIdx.x * P + g; item < a.items; item += (int64_t)gridDim.x * P) {
-    const int64_t t = item / a.head_chunks;
+    const int64_t t = div_index(item, a.head_chunks, a.items32);
     const int h0 = (int)(item - t * a.head_chunks) * U;
     const int n = min(U, (int)a.N - h0);
     TX* xrow = x + (t * a.N + h0) * a.D + a.start + (int64_t)c * VEC;
-    const int64_t b = t / a.S;
+    const int64_t b = div_index(t, a.S, a.items32);
     const int64_t coff = (b * a.cs_b + (t - b * a.S) * a.cs_s) * a.L + (int64_t)c * VEC;
     // ---- issue the loads of the item's rows (and, per head, of their cos/sin)
     Vec<TX, VEC> xv[U][NV];
@@ -234,6 +235,7 @@ cudaError_t launch_vec_kernel(const InplaceProblem& p, cudaStream_t stream) {
   a.chunks = (int32_t)((HALF ? p.L / 2 : p.L) / VEC);
   a.head_chunks = (int32_t)((p.N + U - 1) / U);
   a.items = p.B * p.S * a.head_chunks;
+  a.items32 = a.items <= 0xffffffffLL;
   // a row group needs C threads: the block has at least kThreads and at least C
   const int threads = a.chunks > kThreads ? a.chunks : kThreads;
   const int64_t groups = threads / a.chunks;
