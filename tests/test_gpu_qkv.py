@@ -105,3 +105,27 @@ def test_padding_slots_write_nothing(rope_gpu):
     qg, kg, vg = _run_gpu(case)
     assert same_bits(kg, case.k_cache) and same_bits(vg, case.v_cache)
     _check(case, (qg, kg, vg), _run_oracle(case))
+
+
+def test_empty_sequences(rope_gpu):
+    """Sequences with no new tokens (queryStartLoc repeats a value) sit between
+    non-empty ones; the batch search must skip them."""
+    case = W.qkv_case("empty", 135, [5, 0, 0, 3, 0, 7, 0], [0, 4, 0, 10, 2, 30, 9], 4, 2, 2, 128, 8,
+                      torch.bfloat16)
+    bp, bs = _check(case, _run_gpu(case), _run_oracle(case))
+    assert bp == 0 and bs == 0 and R.get_device_error() == 0
+
+
+@pytest.mark.parametrize("num_seqs", [2047, 2048, 2500])
+def test_many_sequences(rope_gpu, num_seqs):
+    """Up to 2047 sequences the batch tables sit in shared memory; from 2048 on
+    the kernel searches queryStartLoc and seqLens in global memory."""
+    rng = np.random.default_rng(num_seqs)
+    query_lens = [1] * num_seqs
+    for b in rng.choice(num_seqs, 8, replace=False):
+        query_lens[int(b)] = int(rng.integers(2, 40))
+    query_lens[int(rng.integers(num_seqs))] = 0
+    context_lens = [int(v) for v in rng.integers(0, 300, num_seqs)]
+    case = W.qkv_case("many", 136, query_lens, context_lens, 4, 2, 1, 64, 16, torch.float16, pad_every=11)
+    bp, bs = _check(case, _run_gpu(case), _run_oracle(case))
+    assert bp == 0 and bs == 0 and R.get_device_error() == 0
