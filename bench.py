@@ -302,6 +302,9 @@ def run_ours(args):
     # ---- rows beyond the hot path (backward, half mode), each timed cold: a
     # large cache-op launch runs between two of them and flushes their data from L2
     next_rows = time_next_rows(cases, dev_tensors, calls, Kk)
+    streams = time_streams(cases, dev_tensors)
+    for entry in next_rows:
+        entry.update(streams.get(entry["workload"], {}))
     sampler.stop()
     clocks = sampler.summary(t_host0, t_host1)
     ms_step_local = total_ms / K
@@ -317,7 +320,7 @@ def run_ours(args):
                         "avg_us": round(avg * 1e3, 3),
                         "median_us": round(statistics.median(ms) * 1e3, 3),
                         "gbs": round(b / (avg * 1e-3) / 1e9, 1), "frac_of_peak": round(b / (avg * 1e-3) / 1e9 / peak, 4),
-                        "tokens": c.tokens})
+                        "tokens": c.tokens, **streams.get(kernel_label(c), {})})
     dom = max(range(nk), key=lambda i: sum(per_kernel_ms[i]))
     dom_avg_s = sum(per_kernel_ms[dom]) / Kk * 1e-3
     achieved = step_bytes[dom] / dom_avg_s / 1e9
@@ -325,7 +328,8 @@ def run_ours(args):
                 "peak": peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"
                 if peak_kind == "measured" else "fallback", "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel_label(cases[dom])),
-                "algorithmic_bytes": step_bytes[dom]}
+                "algorithmic_bytes": step_bytes[dom],
+                "frac_stream": streams.get(kernel_label(cases[dom]), {}).get("stream_frac_of_peak")}
 
     e2e = run_e2e(args, cases, dev_tensors, calls, world, dev, total_bytes)
 
@@ -350,6 +354,90 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def time_streams(cases, dev_tensors, launches=200):
+    """Steady-state time per launch of each operator in a stream of its own
+    launches: back to back (launches overlap through programmatic stream
+    serialization, as in the step), with events only at the two ends, cycling
+    over enough copies of the operator's buffers that at least 3x the L2
+    capacity of other data passes between two uses of one copy.  Read-only
+    tables (positions, cos/sin, gammas) are shared, as in serving."""
+    import math
+    import transformer_rope_positional_gb300 as R
+    import workloads as W
+    inplace, neox, gptj, mrope = cases
+    x, cs, sn = dev_tensors[0]
+    p3, q3, k3, c3 = dev_tensors[1]
+    p4, q4, k4, c4 = dev_tensors[2]
+    p5, q5, k5, c5 = dev_tensors[3]
+
+    def copies(*ts, n):
+        return [ts] + [tuple(t.clone() for t in ts) for _ in range(n - 1)]
+
+    def sets_for(nbytes):
+        return max(2, math.ceil(3 * L2_BYTES / nbytes) + 1)
+
+    specs = []  # (label, bytes per launch, factory(n) -> list of n prepared calls)
+    ib = algorithmic_bytes(inplace)
+    sl = [inplace.start, inplace.end]
+    specs.append((kernel_label(inplace), ib, lambda n: [R.prepare_inplace_partial(t[0], cs, sn, 1, sl)
+                                                         for t in copies(x, n=n)]))
+    for c, (p, q, k, cc) in ((neox, dev_tensors[1]), (gptj, dev_tensors[2]), (mrope, dev_tensors[3])):
+        specs.append((kernel_label(c), algorithmic_bytes(c),
+                      lambda n, c=c, p=p, q=q, k=k, cc=cc: [
+                          R.prepare_with_sin_cos_cache(p, t[0], t[1], cc, c.head_size, c.rotary_dim, c.is_neox,
+                                                       c.mrope_section) for t in copies(q, k, n=n)]))
+    tag = inplace.name.split("_", 1)[1]
+    specs.append(("inplace_backward_interleave_" + tag, ib, lambda n: [
+        R.prepare_inplace_partial(t[0], cs, sn, 1, sl, backward=True) for t in copies(x, n=n)]))
+    specs.append(("inplace_half_forward_" + tag, ib, lambda n: [
+        R.prepare_inplace_partial(t[0], cs, sn, 0, sl) for t in copies(x, n=n)]))
+    specs.append(("mrope_interleaved_splice_" + mrope.name.split("_", 1)[1], algorithmic_bytes(mrope), lambda n: [
+        R.prepare_with_sin_cos_cache(p5, t[0], t[1], c5, mrope.head_size, mrope.rotary_dim, True,
+                                     mrope.mrope_section, cache_mode=1) for t in copies(q5, k5, n=n)]))
+    specs.append(("rope_neox_out_of_place_" + neox.name.split("_", 2)[2], algorithmic_bytes(neox), lambda n: [
+        R.prepare_with_sin_cos_cache(p3, t[0], t[1], c3, neox.head_size, neox.rotary_dim, True,
+                                     query_out=t[2], key_out=t[3])
+        for t in copies(q3, k3, torch.empty_like(q3), torch.empty_like(k3), n=n)]))
+    wq, wk = q4.shape[1], k4.shape[1]
+    qkv4 = torch.empty(gptj.tokens, wq + 2 * wk, dtype=q4.dtype, device=q4.device)
+    qkv4[:, :wq].copy_(q4)
+    qkv4[:, wq:wq + wk].copy_(k4)
+    specs.append(("rope_gptj_fused_qkv_views_" + gptj.name.split("_", 2)[2], algorithmic_bytes(gptj), lambda n: [
+        R.prepare_with_sin_cos_cache(p4, t[0][:, :wq], t[0][:, wq:wq + wk], c4, gptj.head_size, gptj.rotary_dim,
+                                     False) for t in copies(qkv4, n=n)]))
+    qc = W.qkv_rmsnorm_rope_bf16()
+    dv = q3.device
+    qt = [t.to(dv) for t in (qc.qkv, qc.q_gamma, qc.k_gamma, qc.cache, qc.seq_lens, qc.query_start_loc,
+                             qc.slot_mapping, qc.q_out, qc.k_cache, qc.v_cache)]
+    specs.append((qc.name, algorithmic_bytes(qc), lambda n: [
+        R.prepare_qkv_rmsnorm_rope_cache(t[0], qc.nq, qc.nk, qc.nv, qt[1], qt[2], qc.eps, qt[3], qt[4], qt[5],
+                                         qt[6], t[1], t[2], t[3])
+        for t in copies(qt[0], qt[7], qt[8], qt[9], n=n)]))
+
+    peak, _ = measured_peak()
+    out = {}
+    for label, nbytes, factory in specs:
+        n = sets_for(nbytes)
+        calls = factory(n)
+        for call in calls:
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(2e6))
+        e0.record()
+        for j in range(launches):
+            calls[j % n]()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / launches * 1e3
+        out[label] = {"stream_us": round(us, 3), "stream_frac_of_peak": round(nbytes / (us * 1e-6) / 1e9 / peak, 4),
+                      "stream_buffer_sets": n}
+        del calls
+        torch.cuda.empty_cache()
+    qkv4 = None
+    return out
 
 
 def time_next_rows(cases, dev_tensors, calls, steps):
