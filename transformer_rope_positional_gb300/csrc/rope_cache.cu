@@ -77,30 +77,45 @@ __device__ __forceinline__ int64_t select_row(int k, int64_t p0, int64_t p1, int
   return k == 0 ? p0 : k == 1 ? p1 : k == 2 ? p2 : p3;
 }
 
-// Steps 1-2 for one token: gather cosSin = cache[positions[t]] and split it
-// into this thread's NC cos and NC sin values (first owned index i0).
-// Returns false (nothing loaded) when a position is outside [0, maxSeqLen).
 // How the cos/sin chunk is assembled: plain rope, mrope with the sections
 // spliced in order, mrope with the V2 interleaved splice.
 enum Splice : int { kRope = 0, kSectioned = 1, kInterleaved = 2 };
 
+// The position rows of one token (rope: p[0] only; mrope: 3 or 4 rows).
+struct TokenPos {
+  int64_t p[4];
+};
+
+template <int SPLICE>
+__device__ __forceinline__ TokenPos load_positions(const int64_t* __restrict__ pos, const CacheArgs& a, int64_t t) {
+  TokenPos r;
+  r.p[0] = __ldg(pos + t);
+  if constexpr (SPLICE == kRope) {
+    r.p[1] = r.p[2] = r.p[3] = 0;
+  } else {
+    r.p[1] = __ldg(pos + a.T + t);
+    r.p[2] = __ldg(pos + 2 * a.T + t);
+    r.p[3] = a.mrope_rows > 3 ? __ldg(pos + 3 * a.T + t) : 0;
+  }
+  return r;
+}
+
+// Steps 1-2 for one token: gather cosSin = cache[positions[t]] and split it
+// into this thread's NC cos and NC sin values (first owned index i0).
+// Returns false (nothing loaded) when a position is outside [0, maxSeqLen).
 template <typename T, int NC, int SPLICE>
-__device__ __forceinline__ bool gather_cos_sin(const int64_t* __restrict__ pos, const T* __restrict__ cache,
-                                               const CacheArgs& a, int64_t t, int i0, float (&cf)[NC],
-                                               float (&sf)[NC]) {
+__device__ __forceinline__ bool gather_cos_sin(const TokenPos& tp, const T* __restrict__ cache, const CacheArgs& a,
+                                               int i0, float (&cf)[NC], float (&sf)[NC]) {
   const int half = a.R / 2;
   if constexpr (SPLICE == kRope) {
-    const int64_t p = __ldg(pos + t);
+    const int64_t p = tp.p[0];
     if (p < 0 || p >= a.max_seq) return false;
     const T* rowp = cache + p * a.R;
     load_f32<T, NC>(cf, rowp + i0);
     load_f32<T, NC>(sf, rowp + half + i0);
     return true;
   }
-  const int64_t p0 = __ldg(pos + t);
-  const int64_t p1 = __ldg(pos + a.T + t);
-  const int64_t p2 = __ldg(pos + 2 * a.T + t);
-  const int64_t p3 = a.mrope_rows > 3 ? __ldg(pos + 3 * a.T + t) : 0;
+  const int64_t p0 = tp.p[0], p1 = tp.p[1], p2 = tp.p[2], p3 = tp.p[3];
   if (p0 < 0 || p0 >= a.max_seq || p1 < 0 || p1 >= a.max_seq || p2 < 0 || p2 >= a.max_seq || p3 < 0 ||
       p3 >= a.max_seq)
     return false;
@@ -157,9 +172,24 @@ __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
   const int heads = a.hq + a.hk;
   wait_for_prior_grid();
 
-  // item = (token t, head chunk j): heads [j*U, min(j*U + U, heads)) of token t
-  for (int64_t item = (int64_t)blockIdx.x * P + g; item < a.items; item += (int64_t)gridDim.x * P) {
-    const int64_t t = div_index(item, a.head_chunks, a.items32);
+  // item = (token t, head chunk j): heads [j*U, min(j*U + U, heads)) of token t.
+  // PREFETCH: the next item's position rows are loaded while this item is
+  // processed, so the cos/sin gather leaves with the row loads (measured faster
+  // for the in-place NeoX kernels; the GPT-J and out-of-place kernels lose an
+  // occupancy step to the extra registers and are faster without it).
+  constexpr bool PREFETCH = NEOX && !OUT;
+  const int64_t stride = (int64_t)gridDim.x * P;
+  int64_t item = (int64_t)blockIdx.x * P + g;
+  int64_t t = 0;
+  TokenPos tp{};
+  if constexpr (PREFETCH) {
+    if (item < a.items) {
+      t = div_index(item, a.head_chunks, a.items32);
+      tp = load_positions<SPLICE>(pos, a, t);
+    }
+  }
+  for (; item < a.items; item += stride) {
+    if constexpr (!PREFETCH) t = div_index(item, a.head_chunks, a.items32);
     const int h0 = (int)(item - t * a.head_chunks) * U;
     const int n = min(U, heads - h0);
     // ---- issue the loads of the chunk's rows
@@ -180,8 +210,18 @@ __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
       }
     }
     // ---- steps 1-2: the token's cos/sin chunk
+    if constexpr (!PREFETCH) tp = load_positions<SPLICE>(pos, a, t);
     float cf[NC], sf[NC];
-    if (!gather_cos_sin<T, NC, SPLICE>(pos, cache, a, t, i0, cf, sf)) {
+    const bool in_range = gather_cos_sin<T, NC, SPLICE>(tp, cache, a, i0, cf, sf);
+    const int64_t tt = t;
+    if constexpr (PREFETCH) {  // the next item's token and position rows
+      const int64_t next = item + stride;
+      if (next < a.items) {
+        t = div_index(next, a.head_chunks, a.items32);
+        tp = load_positions<SPLICE>(pos, a, t);
+      }
+    }
+    if (!in_range) {
       // reported once per token, by thread 0 of the group holding head 0
       if (c == 0 && h0 == 0) atomicOr(&g_device_error, kPositionOutOfRange);
       continue;  // leave the token untouched
@@ -193,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
       T* dst = base[u];
       if constexpr (OUT) {
         const int h = h0 + u;
-        dst = h < a.hq ? qo + (t * a.hq + h) * (int64_t)a.head_size
-                       : ko + (t * a.hk + (h - a.hq)) * (int64_t)a.head_size;
+        dst = h < a.hq ? qo + (tt * a.hq + h) * (int64_t)a.head_size
+                       : ko + (tt * a.hk + (h - a.hq)) * (int64_t)a.head_size;
       }
       if constexpr (NEOX) {
 #pragma unroll
