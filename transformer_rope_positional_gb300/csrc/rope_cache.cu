@@ -45,6 +45,9 @@ namespace {
 #ifndef ROPE_CACHE_THREADS
 #define ROPE_CACHE_THREADS 128
 #endif
+#ifndef ROPE_CACHE_MIN_BLOCKS_GPTJ
+#define ROPE_CACHE_MIN_BLOCKS_GPTJ 10
+#endif
 constexpr int kRowsInFlight = ROPE_CACHE_ROWS_IN_FLIGHT;  // U: rows loaded before compute, per thread
 constexpr int kThreads = ROPE_CACHE_THREADS;
 constexpr unsigned kPositionOutOfRange = 1u;
@@ -80,6 +83,15 @@ __device__ __forceinline__ int64_t select_row(int k, int64_t p0, int64_t p1, int
 // How the cos/sin chunk is assembled: plain rope, mrope with the sections
 // spliced in order, mrope with the V2 interleaved splice.
 enum Splice : int { kRope = 0, kSectioned = 1, kInterleaved = 2 };
+
+// CTAs per SM asked of the compiler.  The in-place GPT-J rope kernel (one
+// vector per row and thread, a quarter of each row touched) is latency-bound:
+// 10 CTAs (48 registers, no spills) beat its uncapped 7; the other variants are
+// best uncapped (a cap spills them).
+template <bool NEOX, bool OUT, int SPLICE>
+__host__ __device__ constexpr int min_blocks() {
+  return (!NEOX && !OUT && SPLICE == kRope) ? ROPE_CACHE_MIN_BLOCKS_GPTJ : ROPE_CACHE_MIN_BLOCKS;
+}
 
 // The position rows of one token (rope: p[0] only; mrope: 3 or 4 rows).
 struct TokenPos {
@@ -157,7 +169,7 @@ __device__ __forceinline__ bool gather_cos_sin(const TokenPos& tp, const T* __re
 // OUT: results go to the contiguous outputs qo/ko (pass-through columns
 // copied there); otherwise query/key are rewritten in place.
 template <typename T, bool NEOX, bool OUT, int SPLICE, int VEC>
-__global__ void __launch_bounds__(kThreads, ROPE_CACHE_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, min_blocks<NEOX, OUT, SPLICE>())
     cache_kernel(const int64_t* __restrict__ pos, T* __restrict__ q, T* __restrict__ k,
                  const T* __restrict__ cache, T* __restrict__ qo, T* __restrict__ ko, CacheArgs a) {
   constexpr int U = kRowsInFlight;
