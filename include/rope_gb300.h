@@ -213,15 +213,22 @@ int rope_with_sin_cos_cache_v2(const rope_tensor_t* positions, const rope_tensor
  *                  or 16 (F32), at most 512 (F16/BF16) or 256 (F32).
  *   q_gamma, k_gamma  [D], same dtype.      eps >= 0 (added to the mean of squares).
  *   cos_sin_cache  [maxSeq, D], same dtype: cos in the first half of a row, sin in the second.
- *   seq_lens       I64 [B]: tokens of each sequence including this call's;
- *   query_start_loc I64 [B + 1]: first token of each batch in qkv (last entry T);
+ *   seq_lens       I64 [B]: tokens of each sequence including this call's; 1 <= B <= 2^30;
+ *   query_start_loc I64 [B + 1]: first token of each batch in qkv, non-decreasing, from 0
+ *                  to T (a batch may be empty).  Other values cannot make the kernel
+ *                  access memory outside the tensors, but which batch a token is given
+ *                  to is then unspecified;
  *   slot_mapping   I64 [T]: cache slot of each token; a negative slot writes no cache
  *                  (padding).
  *   q_out          [T, Nq * D] output; k_cache [NB, Nk, BS, D] and v_cache [NB, Nv, BS, D]
  *                  are updated in place at the tokens' slots only.
  * All float tensors 16-byte aligned, int64 tensors 8-byte aligned, all contiguous.
- * Computed in binary32 (mean of squares, reciprocal square root, products, the
- * rotation as in rope_with_sin_cos_cache) and rounded once per output element.
+ * Computed in binary32 and rounded once per output element: the mean of squares, the
+ * reciprocal square root, and the rotation with gamma folded into cos/sin,
+ *   r_lo = (x_lo*(g_lo*cos) - x_hi*(g_hi*sin)) / rms,  r_hi = (x_hi*(g_hi*cos) + x_lo*(g_lo*sin)) / rms,
+ * each a product, an FMA and the scaling (the terms already carry one rounding of
+ * the normalisation, so the compensated difference of rope_with_sin_cos_cache would
+ * not make the result more accurate).
  * A token whose position falls outside the table writes nothing and records
  * ROPE_DEVICE_POSITION_OUT_OF_RANGE; a slot at or past NB * BS writes no cache and
  * records ROPE_DEVICE_SLOT_OUT_OF_RANGE (q_out is still written).

@@ -267,7 +267,8 @@ int qkv_call(const rope_tensor_t* qkv, int64_t nq, int64_t nk, int64_t nv, const
     return ROPE_ERR_PARAM_INVALID;
   if (cache->ndim != 2 || cache->shape[1] != D || cache->shape[0] < 1) return ROPE_ERR_PARAM_INVALID;
   const int64_t B = seq_lens->shape[0];
-  if (B < 1 || qsl->shape[0] != B + 1 || slot_mapping->shape[0] != T) return ROPE_ERR_PARAM_INVALID;
+  if (B < 1 || B > (int64_t(1) << 30) || qsl->shape[0] != B + 1 || slot_mapping->shape[0] != T)
+    return ROPE_ERR_PARAM_INVALID;
   if (q_out->ndim != 2 || q_out->shape[0] != T || q_out->shape[1] != nq * D) return ROPE_ERR_PARAM_INVALID;
   if (k_cache->ndim != 4 || v_cache->ndim != 4) return ROPE_ERR_PARAM_INVALID;
   const int64_t NB = k_cache->shape[0], BS = k_cache->shape[2];
