@@ -221,7 +221,8 @@ int rope_with_sin_cos_cache_v2(const rope_tensor_t* positions, const rope_tensor
  *   slot_mapping   I64 [T]: cache slot of each token; a negative slot writes no cache
  *                  (padding).
  *   q_out          [T, Nq * D] output; k_cache [NB, Nk, BS, D] and v_cache [NB, Nv, BS, D]
- *                  are updated in place at the tokens' slots only.
+ *                  are updated in place at the tokens' slots only.  Nq + Nk + Nv and BS
+ *                  are at most 2^30.
  * All float tensors 16-byte aligned, int64 tensors 8-byte aligned, all contiguous.
  * Computed in binary32 and rounded once per output element: the mean of squares, the
  * reciprocal square root, and the rotation with gamma folded into cos/sin,

@@ -285,6 +285,8 @@ def _qkv(lib, **over):
     (dict(qsl=_d(C.I64, (2,))), C.ROPE_ERR_PARAM_INVALID),          # query_start_loc length != B + 1
     (dict(slots=_d(C.I64, (5,))), C.ROPE_ERR_PARAM_INVALID),        # one slot per token
     (dict(sl=_d(C.I64, ((1 << 30) + 1,)), qsl=_d(C.I64, ((1 << 30) + 2,))), C.ROPE_ERR_PARAM_INVALID),  # > 2^30 seqs
+    (dict(kc=_d(C.BF16, (1, 1, (1 << 30) + 1, 64)), vc=_d(C.BF16, (1, 1, (1 << 30) + 1, 64))),
+     C.ROPE_ERR_PARAM_INVALID),  # block size past 2^30
     (dict(qo=_d(C.BF16, (6, 64))), C.ROPE_ERR_PARAM_INVALID),       # q_out width
     (dict(vc=_d(C.BF16, (3, 1, 8, 64))), C.ROPE_ERR_PARAM_INVALID),  # block sizes differ
     (dict(eps=-1.0), C.ROPE_ERR_PARAM_INVALID),

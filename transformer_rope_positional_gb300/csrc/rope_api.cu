@@ -275,6 +275,8 @@ int qkv_call(const rope_tensor_t* qkv, int64_t nq, int64_t nk, int64_t nv, const
   if (NB < 1 || BS < 1 || k_cache->shape[1] != nk || k_cache->shape[3] != D || v_cache->shape[0] != NB ||
       v_cache->shape[1] != nv || v_cache->shape[2] != BS || v_cache->shape[3] != D)
     return ROPE_ERR_PARAM_INVALID;
+  // head counts and the block size are kept in 32-bit fields by the kernel
+  if (nq + nk + nv > (int64_t(1) << 30) || BS > (int64_t(1) << 30)) return ROPE_ERR_PARAM_INVALID;
   if (!(eps >= 0.0f) || !(eps < 1e30f)) return ROPE_ERR_PARAM_INVALID;
   for (const rope_tensor_t* t : all)
     if (!t->data && numel(t) > 0) return ROPE_ERR_PARAM_NULLPTR;
