@@ -57,3 +57,32 @@ def test_graph_capture_and_replay(rope_gpu):
             for (_, q, k, _), (qo, ko) in zip(ins, qr):
                 assert ulp_distance(q.cpu(), qo).max() <= 2 and ulp_distance(k.cpu(), ko).max() <= 2
     assert R.get_device_error() == 0
+
+
+def test_graph_fused_qkv(rope_gpu):
+    """The fused op (dynamic shared memory for its batch tables) captured and
+    replayed: outputs as the oracle's."""
+    from test_gpu_qkv import _check, _run_oracle
+    case = W.qkv_case("graph_qkv", 144, [37, 1, 1, 64, 3], [0, 100, 5, 30, 200], 4, 2, 2, 128, 16,
+                      torch.bfloat16, pad_every=7)
+    d = lambda t: t.cuda()  # noqa: E731
+    ins = [d(t) for t in (case.qkv, case.q_gamma, case.k_gamma, case.cache, case.seq_lens, case.query_start_loc,
+                          case.slot_mapping)]
+    qo, kc, vc = d(case.q_out), d(case.k_cache), d(case.v_cache)
+    qo0, kc0, vc0 = qo.clone(), kc.clone(), vc.clone()
+    R.load()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            R.qkv_rmsnorm_rope_cache(ins[0], case.nq, case.nk, case.nv, ins[1], ins[2], case.eps, ins[3], ins[4],
+                                     ins[5], ins[6], qo, kc, vc)
+    torch.cuda.synchronize()
+    for t, t0 in ((qo, qo0), (kc, kc0), (vc, vc0)):
+        t.copy_(t0)
+    for _ in range(2):  # the op does not read its outputs: replaying twice gives the same result
+        graph.replay()
+    torch.cuda.synchronize()
+    _check(case, (qo.cpu(), kc.cpu(), vc.cpu()), _run_oracle(case))
+    assert R.get_device_error() == 0
