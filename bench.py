@@ -301,8 +301,10 @@ def run_ours(args):
 
     # ---- rows beyond the hot path (backward, half mode), each timed cold: a
     # large cache-op launch runs between two of them and flushes their data from L2
-    next_rows = time_next_rows(cases, dev_tensors, calls, Kk)
-    streams = time_streams(cases, dev_tensors)
+    specs = operator_specs(cases, dev_tensors)
+    next_rows = time_next_rows(specs, calls, Kk)
+    streams = time_streams(specs)
+    del specs
     for entry in next_rows:
         entry.update(streams.get(entry["workload"], {}))
     sampler.stop()
@@ -365,14 +367,22 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_streams(cases, dev_tensors, launches=200):
-    """Steady-state time per launch of each operator in a stream of its own
-    launches: back to back (launches overlap through programmatic stream
-    serialization, as in the step), with events only at the two ends, cycling
-    over enough copies of the operator's buffers that at least 3x the L2
-    capacity of other data passes between two uses of one copy.  Read-only
-    tables (positions, cos/sin, gammas) are shared, as in serving."""
-    import math
+def copies(*ts, n):
+    """The given tensors, then n - 1 clones of them (the originals come first)."""
+    return [ts] + [tuple(t.clone() for t in ts) for _ in range(n - 1)]
+
+
+def operator_specs(cases, dev_tensors):
+    """Every operator timed by the bench, as (label, algorithmic bytes per
+    launch, factory, flush index): factory(n) prepares n launches on n copies of
+    the operator's buffers (the first on the step's own tensors); read-only
+    tables (positions, cos/sin, gammas) are shared, as in serving.  The first
+    four are the hot-path kernels of the step, the rest the rows beyond it: the
+    in-place operator's backward and half mode, the V2 cache operator with the
+    interleaved mrope splice, with separate outputs and on strided views of a
+    fused QKV buffer, and the fused QKV split + RMSNorm + RoPE + paged cache
+    write.  The flush index names the step kernel (NeoX 1 or mrope 3) whose
+    launch on other buffers evicts a row's data between its evented launches."""
     import transformer_rope_positional_gb300 as R
     import workloads as W
     inplace, neox, gptj, mrope = cases
@@ -380,55 +390,58 @@ def time_streams(cases, dev_tensors, launches=200):
     p3, q3, k3, c3 = dev_tensors[1]
     p4, q4, k4, c4 = dev_tensors[2]
     p5, q5, k5, c5 = dev_tensors[3]
-
-    def copies(*ts, n):
-        return [ts] + [tuple(t.clone() for t in ts) for _ in range(n - 1)]
-
-    def sets_for(nbytes):
-        return max(2, math.ceil(3 * L2_BYTES / nbytes) + 1)
-
-    specs = []  # (label, bytes per launch, factory(n) -> list of n prepared calls)
     ib = algorithmic_bytes(inplace)
     sl = [inplace.start, inplace.end]
-    specs.append((kernel_label(inplace), ib, lambda n: [R.prepare_inplace_partial(t[0], cs, sn, 1, sl)
-                                                         for t in copies(x, n=n)]))
+    specs = [(kernel_label(inplace), ib, lambda n: [R.prepare_inplace_partial(t[0], cs, sn, 1, sl)
+                                                     for t in copies(x, n=n)], None)]
     for c, (p, q, k, cc) in ((neox, dev_tensors[1]), (gptj, dev_tensors[2]), (mrope, dev_tensors[3])):
         specs.append((kernel_label(c), algorithmic_bytes(c),
                       lambda n, c=c, p=p, q=q, k=k, cc=cc: [
                           R.prepare_with_sin_cos_cache(p, t[0], t[1], cc, c.head_size, c.rotary_dim, c.is_neox,
-                                                       c.mrope_section) for t in copies(q, k, n=n)]))
+                                                       c.mrope_section) for t in copies(q, k, n=n)], None))
     tag = inplace.name.split("_", 1)[1]
     specs.append(("inplace_backward_interleave_" + tag, ib, lambda n: [
-        R.prepare_inplace_partial(t[0], cs, sn, 1, sl, backward=True) for t in copies(x, n=n)]))
+        R.prepare_inplace_partial(t[0], cs, sn, 1, sl, backward=True) for t in copies(x, n=n)], 1))
     specs.append(("inplace_half_forward_" + tag, ib, lambda n: [
-        R.prepare_inplace_partial(t[0], cs, sn, 0, sl) for t in copies(x, n=n)]))
+        R.prepare_inplace_partial(t[0], cs, sn, 0, sl) for t in copies(x, n=n)], 3))
     specs.append(("mrope_interleaved_splice_" + mrope.name.split("_", 1)[1], algorithmic_bytes(mrope), lambda n: [
         R.prepare_with_sin_cos_cache(p5, t[0], t[1], c5, mrope.head_size, mrope.rotary_dim, True,
-                                     mrope.mrope_section, cache_mode=1) for t in copies(q5, k5, n=n)]))
+                                     mrope.mrope_section, cache_mode=1) for t in copies(q5, k5, n=n)], 1))
+    # NeoX workload, R == head size: no pass-through columns to copy
+    qo, ko = torch.empty_like(q3), torch.empty_like(k3)
     specs.append(("rope_neox_out_of_place_" + neox.name.split("_", 2)[2], algorithmic_bytes(neox), lambda n: [
         R.prepare_with_sin_cos_cache(p3, t[0], t[1], c3, neox.head_size, neox.rotary_dim, True,
-                                     query_out=t[2], key_out=t[3])
-        for t in copies(q3, k3, torch.empty_like(q3), torch.empty_like(k3), n=n)]))
+                                     query_out=t[2], key_out=t[3]) for t in copies(q3, k3, qo, ko, n=n)], 3))
+    # GPT-J workload on q/k views of a fused [T, (16+16+16)*256] QKV buffer
     wq, wk = q4.shape[1], k4.shape[1]
     qkv4 = torch.empty(gptj.tokens, wq + 2 * wk, dtype=q4.dtype, device=q4.device)
     qkv4[:, :wq].copy_(q4)
     qkv4[:, wq:wq + wk].copy_(k4)
     specs.append(("rope_gptj_fused_qkv_views_" + gptj.name.split("_", 2)[2], algorithmic_bytes(gptj), lambda n: [
         R.prepare_with_sin_cos_cache(p4, t[0][:, :wq], t[0][:, wq:wq + wk], c4, gptj.head_size, gptj.rotary_dim,
-                                     False) for t in copies(qkv4, n=n)]))
+                                     False) for t in copies(qkv4, n=n)], 1))
+    # mixed prefill/decode batch
     qc = W.qkv_rmsnorm_rope_bf16()
-    dv = q3.device
-    qt = [t.to(dv) for t in (qc.qkv, qc.q_gamma, qc.k_gamma, qc.cache, qc.seq_lens, qc.query_start_loc,
-                             qc.slot_mapping, qc.q_out, qc.k_cache, qc.v_cache)]
+    qt = [t.to(q3.device) for t in (qc.qkv, qc.q_gamma, qc.k_gamma, qc.cache, qc.seq_lens, qc.query_start_loc,
+                                    qc.slot_mapping, qc.q_out, qc.k_cache, qc.v_cache)]
     specs.append((qc.name, algorithmic_bytes(qc), lambda n: [
         R.prepare_qkv_rmsnorm_rope_cache(t[0], qc.nq, qc.nk, qc.nv, qt[1], qt[2], qc.eps, qt[3], qt[4], qt[5],
                                          qt[6], t[1], t[2], t[3])
-        for t in copies(qt[0], qt[7], qt[8], qt[9], n=n)]))
+        for t in copies(qt[0], qt[7], qt[8], qt[9], n=n)], 3))
+    return specs
 
+
+def time_streams(specs, launches=200):
+    """Steady-state time per launch of each operator in a stream of its own
+    launches: back to back (launches overlap through programmatic stream
+    serialization, as in the step), with events only at the two ends, cycling
+    over enough copies of the operator's buffers that at least 3x the L2
+    capacity of other data passes between two uses of one copy."""
+    import math
     peak, _ = measured_peak()
     out = {}
-    for label, nbytes, factory in specs:
-        n = sets_for(nbytes)
+    for label, nbytes, factory, _ in specs:
+        n = max(2, math.ceil(3 * L2_BYTES / nbytes) + 1)
         calls = factory(n)
         for call in calls:
             call()
@@ -445,54 +458,14 @@ def time_streams(cases, dev_tensors, launches=200):
                       "stream_buffer_sets": n}
         del calls
         torch.cuda.empty_cache()
-    qkv4 = None
     return out
 
 
-def time_next_rows(cases, dev_tensors, calls, steps):
+def time_next_rows(specs, calls, steps):
     """Per-launch time of the rows beyond the hot path on the hot path's own
-    workloads: the in-place operator's backward and half mode, the V2 cache
-    operator with the interleaved mrope splice, with separate outputs, and on
-    strided views of a fused QKV buffer.  Each timed launch is followed by a
-    large cache-op launch on other buffers, so every timed launch starts cold."""
-    import transformer_rope_positional_gb300 as R
-    inplace, neox, gptj, mrope = cases
-    x, cs, sn = dev_tensors[0]
-    p3, q3, k3, c3 = dev_tensors[1]
-    p4, q4, k4, c4 = dev_tensors[2]
-    p5, q5, k5, c5 = dev_tensors[3]
-    tag = inplace.name.split("_", 1)[1]
-    rows = [("inplace_backward_interleave_" + tag, algorithmic_bytes(inplace),
-             R.prepare_inplace_partial(x, cs, sn, 1, [inplace.start, inplace.end], backward=True), calls[1]),
-            ("inplace_half_forward_" + tag, algorithmic_bytes(inplace),
-             R.prepare_inplace_partial(x, cs, sn, 0, [inplace.start, inplace.end]), calls[3])]
-    # V2 interleaved splice on the mrope workload
-    rows.append(("mrope_interleaved_splice_" + mrope.name.split("_", 1)[1], algorithmic_bytes(mrope),
-                 R.prepare_with_sin_cos_cache(p5, q5, k5, c5, mrope.head_size, mrope.rotary_dim, True,
-                                              mrope.mrope_section, cache_mode=1), calls[1]))
-    # V2 separate outputs on the NeoX workload (R == head size: no pass-through)
-    qo, ko = torch.empty_like(q3), torch.empty_like(k3)
-    rows.append(("rope_neox_out_of_place_" + neox.name.split("_", 2)[2], algorithmic_bytes(neox),
-                 R.prepare_with_sin_cos_cache(p3, q3, k3, c3, neox.head_size, neox.rotary_dim, True,
-                                              query_out=qo, key_out=ko), calls[3]))
-    # V2 strided rows: GPT-J workload on q/k views of a fused [T, (16+16+16)*256] QKV buffer
-    T, hs = gptj.tokens, gptj.head_size
-    wq, wk = q4.shape[1], k4.shape[1]
-    qkv = torch.empty(T, wq + wk + wk, dtype=q4.dtype, device=q4.device)
-    qkv[:, :wq].copy_(q4)
-    qkv[:, wq:wq + wk].copy_(k4)
-    rows.append(("rope_gptj_fused_qkv_views_" + gptj.name.split("_", 2)[2], algorithmic_bytes(gptj),
-                 R.prepare_with_sin_cos_cache(p4, qkv[:, :wq], qkv[:, wq:wq + wk], c4, hs, gptj.rotary_dim, False),
-                 calls[1]))
-    # fused QKV split + RMSNorm + RoPE + paged cache write (mixed prefill/decode batch)
-    import workloads as W
-    qc = W.qkv_rmsnorm_rope_bf16()
-    dv = q3.device
-    qt = [t.to(dv) for t in (qc.qkv, qc.q_gamma, qc.k_gamma, qc.cache, qc.seq_lens, qc.query_start_loc,
-                             qc.slot_mapping, qc.q_out, qc.k_cache, qc.v_cache)]
-    rows.append((qc.name, algorithmic_bytes(qc),
-                 R.prepare_qkv_rmsnorm_rope_cache(qt[0], qc.nq, qc.nk, qc.nv, qt[1], qt[2], qc.eps, qt[3], qt[4],
-                                                  qt[5], qt[6], qt[7], qt[8], qt[9]), calls[3]))
+    workloads, each launch between two events and followed by a launch of a
+    large step kernel on other buffers, so every timed launch starts cold."""
+    rows = [(name, b, factory(1)[0], calls[flush]) for name, b, factory, flush in specs if flush is not None]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(rows))] for _ in range(steps)]
     for _ in range(3):
         for _, _, call, flush in rows:
