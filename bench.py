@@ -437,28 +437,34 @@ def time_streams(specs, launches=200):
     serialization, as in the step), with events only at the two ends, cycling
     over enough copies of the operator's buffers that at least 3x the L2
     capacity of other data passes between two uses of one copy."""
-    import math
     peak, _ = measured_peak()
     out = {}
     for label, nbytes, factory, _ in specs:
-        n = max(2, math.ceil(3 * L2_BYTES / nbytes) + 1)
-        calls = factory(n)
-        for call in calls:
-            call()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda._sleep(int(2e6))
-        e0.record()
-        for j in range(launches):
-            calls[j % n]()
-        e1.record()
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) / launches * 1e3
+        us, n = stream_us(factory, nbytes, launches)
         out[label] = {"stream_us": round(us, 3), "stream_frac_of_peak": round(nbytes / (us * 1e-6) / 1e9 / peak, 4),
                       "stream_buffer_sets": n}
-        del calls
-        torch.cuda.empty_cache()
     return out
+
+
+def stream_us(factory, nbytes, launches=200):
+    """(microseconds per launch, buffer copies) of back-to-back launches cycling
+    over enough copies that 3x L2 of other data passes between two uses."""
+    import math
+    n = max(2, math.ceil(3 * L2_BYTES / nbytes) + 1)
+    calls = factory(n)
+    for call in calls:
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(2e6))
+    e0.record()
+    for j in range(launches):
+        calls[j % n]()
+    e1.record()
+    torch.cuda.synchronize()
+    del calls
+    torch.cuda.empty_cache()
+    return e0.elapsed_time(e1) / launches * 1e3, n
 
 
 def time_next_rows(specs, calls, steps):
@@ -657,6 +663,73 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_size_sweep(args):
+    """Each operator stream-timed (as in the step's stream region) on its
+    workload at 0.5x, 1x, 1.5x and 2x the tokens, and a least-squares line
+    time = fixed + bytes / rate through the four points: `rate` is the
+    streaming rate of the kernel, `fixed_us` the per-launch cost (ramp-up,
+    drain) that the launch cannot amortise."""
+    import workloads as W
+    from transformer_rope_positional_gb300 import build as B
+    B.build()
+    import transformer_rope_positional_gb300 as R
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, _ = measured_peak()
+
+    def mrope(f):
+        pos = W.mrope_positions(int(8192 * f), (int(6 * f), 64, 64))
+        return W.cache_case("mrope_%dtok" % pos.shape[1], 4, pos.shape[1], 28, 4, 128, 128, 40960, torch.bfloat16,
+                            True, base=1e6, positions=pos, mrope_section=[16, 24, 24])
+
+    def qkv(f):
+        ctx = W.uniform_int(W.stream_seed(5, 3), 256, 16, 1024).tolist()
+        return W.qkv_case("qkv_%dtok" % (4 * int(1984 * f) + 256), 5, [int(1984 * f)] * 4 + [1] * 256,
+                          [4096] * 4 + ctx, 32, 8, 8, 128, 16, torch.bfloat16)
+
+    def factory(c):
+        if hasattr(c, "qkv"):
+            ro = [t.to(dev) for t in (c.q_gamma, c.k_gamma, c.cache, c.seq_lens, c.query_start_loc, c.slot_mapping)]
+            ts = [t.to(dev) for t in (c.qkv, c.q_out, c.k_cache, c.v_cache)]
+            return lambda n: [R.prepare_qkv_rmsnorm_rope_cache(t[0], c.nq, c.nk, c.nv, ro[0], ro[1], c.eps, ro[2],
+                                                               ro[3], ro[4], ro[5], t[1], t[2], t[3])
+                              for t in copies(*ts, n=n)]
+        if hasattr(c, "x"):
+            cs, sn = c.cos.to(dev), c.sin.to(dev)
+            x = c.x.to(dev)
+            return lambda n: [R.prepare_inplace_partial(t[0], cs, sn, 1, [c.start, c.end]) for t in copies(x, n=n)]
+        p, cc = c.positions.to(dev), c.cache.to(dev)
+        q, k = c.query.to(dev), c.key.to(dev)
+        return lambda n: [R.prepare_with_sin_cos_cache(p, t[0], t[1], cc, c.head_size, c.rotary_dim, c.is_neox,
+                                                       c.mrope_section) for t in copies(q, k, n=n)]
+
+    families = [("inplace_bf16x_f32cs_Bx4096x32x128_slice64_128", lambda f: W.inplace_bf16_mixed(int(4 * f))),
+                ("rope_neox_bf16_32q8k_h128", lambda f: W.cache_neox_bf16(int(16384 * f))),
+                ("rope_gptj_f16_16q16k_h256_r64", lambda f: W.cache_gptj_f16_partial(int(8 * f))),
+                ("mrope_neox_bf16_28q4k_h128_s16_24_24", mrope),
+                ("qkv_rmsnorm_rope_bf16_32q8k8v_h128", qkv)]
+    out = []
+    for name, make in families:
+        pts = []
+        for f in (0.5, 1.0, 1.5, 2.0):
+            c = make(f)
+            nbytes = algorithmic_bytes(c)
+            us, _ = stream_us(factory(c), nbytes)
+            pts.append({"tokens": c.tokens, "bytes": nbytes, "us": round(us, 3)})
+            del c
+            torch.cuda.empty_cache()
+        xs = [p["bytes"] for p in pts]
+        ys = [p["us"] for p in pts]
+        mx, my = sum(xs) / len(xs), sum(ys) / len(ys)
+        slope = sum((x - mx) * (y - my) for x, y in zip(xs, ys)) / sum((x - mx) ** 2 for x in xs)  # us per byte
+        rate = 1e-3 / slope  # GB/s
+        out.append({"family": name, "points": pts, "stream_rate_gbs": round(rate, 1),
+                    "stream_rate_frac_of_peak": round(rate / peak, 4), "fixed_us": round(my - slope * mx, 3)})
+        print(json.dumps(out[-1]), flush=True)
+    print(json.dumps({"metric": "stream rate and per-launch fixed cost from a size sweep", "peak_gbs": peak,
+                      "families": out}), flush=True)
+
+
 def run_marginal(args):
     """Each hot-path kernel alone, at its token count and at twice that, with a
     read-only sweep of 384 MB before every launch (clean, cold L2).  Reports the
@@ -723,6 +796,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--marginal", action="store_true",
                     help="instead of the step: each kernel alone at 1x and 2x tokens on a clean L2")
+    ap.add_argument("--size-sweep", action="store_true",
+                    help="instead of the step: each operator stream-timed at 0.5x..2x tokens; rate and fixed cost")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -730,6 +805,8 @@ def main():
         run_reference(args)
     elif args.marginal:
         run_marginal(args)
+    elif args.size_sweep:
+        run_size_sweep(args)
     else:
         run_ours(args)
 
