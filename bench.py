@@ -580,11 +580,17 @@ def oracle_sample(case, tokens: int):
     import workloads as W
     if hasattr(case, "x"):
         B, S, N, D = case.x.shape
-        s = max(1, min(S, tokens))
+        if tokens >= S:  # whole batches (b, s order)
+            nb = min(B, tokens // S)
+            x = case.x[:nb].contiguous()
+            cos = case.cos[:nb].contiguous() if case.cos.shape[0] != 1 else case.cos
+            sin = case.sin[:nb].contiguous() if case.sin.shape[0] != 1 else case.sin
+            return W.InplaceCase(case.name, x, cos, sin, case.start, case.end)
+        s = max(1, tokens)
         x = case.x[:1, :s].contiguous()
-        cos = case.cos[:, :s].contiguous() if case.cos.shape[1] != 1 else case.cos
-        sin = case.sin[:, :s].contiguous() if case.sin.shape[1] != 1 else case.sin
-        return W.InplaceCase(case.name, x, cos[:1], sin[:1], case.start, case.end)
+        cos = case.cos[:1, :s].contiguous() if case.cos.shape[1] != 1 else case.cos[:1]
+        sin = case.sin[:1, :s].contiguous() if case.sin.shape[1] != 1 else case.sin[:1]
+        return W.InplaceCase(case.name, x, cos, sin, case.start, case.end)
     t = max(1, min(case.tokens, tokens))
     return W.CacheCase(case.name, case.positions[..., :t].contiguous(), case.query[:t].contiguous(),
                        case.key[:t].contiguous(), case.cache, case.head_size, case.rotary_dim, case.is_neox,
@@ -626,10 +632,11 @@ def cpu_baseline(cases, budget_s: float):
     secs = time_oracle(samples)
     b = sum(algorithmic_bytes(s) for s in samples)
     tok = sum(s.tokens for s in samples)
+    total_tok = sum(c.tokens for c in cases)
     return {"value": round(b / secs / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "tokens_per_s": round(tok / secs, 1), "seconds": round(secs, 2),
-            "sample": "first %.2f%% of the tokens of each of the four workloads (%d tokens, %d bytes), "
-                      "binary64 scalar C oracle, one thread" % (100 * frac, tok, b)}
+            "sample": "leading tokens of each of the four workloads, %d of the step's %d tokens (%.1f%%), %d bytes; "
+                      "binary64 scalar C oracle, one thread" % (tok, total_tok, 100 * tok / total_tok, b)}
 
 
 def run_reference(args):
@@ -649,8 +656,9 @@ def run_reference(args):
     b = sum(algorithmic_bytes(s) for s in samples)
     tok = sum(s.tokens for s in samples)
     value = b / secs / 1e9
-    sample = ("first %.3f%% of the tokens of each of the four workloads per step (%d tokens, %d bytes), "
-              "binary64 scalar C oracle, one thread" % (100 * frac, tok, b))
+    total_tok = sum(c.tokens for c in cases)
+    sample = ("leading tokens of each of the four workloads per step, %d of the step's %d tokens (%.3f%%), "
+              "%d bytes; binary64 scalar C oracle, one thread" % (tok, total_tok, 100 * tok / total_tok, b))
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
