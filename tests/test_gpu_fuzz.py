@@ -1,0 +1,88 @@
+"""Seeded random parity sweep: shapes, dtypes, slices, cos/sin layouts, modes
+and directions of the in-place operator, and head sizes, rotary dims, styles,
+mrope sections and splices of the cache operator, each case checked against
+the oracle with the tolerances of ``parity.py``.  The cases are drawn from a
+fixed seed per case, so a failure names a reproducible case."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import transformer_rope_positional_gb300 as R
+import workloads as W
+from parity import assert_matches
+
+pytestmark = pytest.mark.gpu
+
+COMBOS = [(torch.float32, torch.float32), (torch.float16, torch.float16), (torch.bfloat16, torch.bfloat16),
+          (torch.float16, torch.float32), (torch.bfloat16, torch.float32)]
+LAYOUTS = ["1S1L", "BS1L", "B11L", "111L", "BSNL", "B1NL", "1SNL"]
+
+
+def _cs_shape(layout, B, S, N, L):
+    return tuple(dict(B=B, S=S, N=N, L=L)[ch] if ch != "1" else 1 for ch in layout)
+
+
+@pytest.mark.parametrize("i", range(100))
+def test_inplace_random_case(rope_gpu, i):
+    rng = np.random.default_rng(7000 + i)
+    xdt, cdt = COMBOS[rng.integers(len(COMBOS))]
+    B, S, N = int(rng.integers(1, 4)), int(rng.integers(1, 60)), int(rng.integers(1, 7))
+    D = 2 * int(rng.integers(1, 129))  # even, up to 256
+    if rng.random() < 0.1:
+        start, end = 0, 0
+        L = D
+    else:
+        start = int(rng.integers(0, D - 1))
+        L = 2 * int(rng.integers(1, (D - start) // 2 + 1))
+        end = start + L
+    layout = LAYOUTS[rng.integers(len(LAYOUTS))]
+    mode = int(rng.integers(0, 2))
+    backward = bool(rng.integers(0, 2))
+    kind = "randn" if "N" in layout else "rotary"
+    case = W.inplace_case("fuzz%d" % i, 7000 + i, (B, S, N, D), start, end, xdt, cdt,
+                          cs_shape=_cs_shape(layout, B, S, N, L), cs_kind=kind)
+    x = case.x.cuda()
+    fn = R.rope_inplace_partial_backward if backward else R.rope_inplace_partial
+    fn(x, case.cos.cuda(), case.sin.cuda(), mode, [start, end])
+    torch.cuda.synchronize()
+    ref = oracle.inplace_partial_rotary_mul(case.x, case.cos, case.sin, start, end, rotary_mode=mode,
+                                            backward=backward)
+    assert_matches(x.cpu(), ref, "case %d: %s %s x%s slice [%d,%d) layout %s mode %d %s" % (
+        i, xdt, cdt, (B, S, N, D), start, end, layout, mode, "bwd" if backward else "fwd"))
+
+
+@pytest.mark.parametrize("i", range(100))
+def test_cache_random_case(rope_gpu, i):
+    rng = np.random.default_rng(8000 + i)
+    dt = [torch.float32, torch.float16, torch.bfloat16][rng.integers(3)]
+    mult = 16 if dt == torch.float32 else 32
+    hs = mult * int(rng.integers(1, 256 // mult + 1))
+    r = mult * int(rng.integers(1, hs // mult + 1))
+    T, hq, hk = int(rng.integers(1, 300)), int(rng.integers(1, 7)), int(rng.integers(1, 5))
+    neox = bool(rng.integers(0, 2))
+    section, cache_mode = None, 0
+    if rng.random() < 0.5:  # mrope: 3 or 4 sections summing to R/2, the first non-zero
+        m = int(rng.integers(3, 5))
+        cuts = np.sort(rng.integers(0, r // 2 + 1, m - 1))
+        section = np.diff(np.concatenate([[0], cuts, [r // 2]])).astype(int).tolist()
+        if section[0] == 0:
+            section[0], section[-1] = section[-1], 0
+        if section[0] == 0:
+            section = None
+        elif m == 3 and rng.random() < 0.5:
+            cache_mode = 1  # V2 interleaved splice (three sections)
+    case = W.cache_case("fuzz%d" % i, 8000 + i, T, hq, hk, hs, r, int(rng.integers(1, 3000)), dt, neox,
+                        mrope_section=section)
+    q, k = case.query.cuda(), case.key.cuda()
+    R.rope_with_sin_cos_cache(case.positions.cuda(), q, k, case.cache.cuda(), hs, r, neox, section,
+                              cache_mode=cache_mode)
+    torch.cuda.synchronize()
+    qo, ko, skipped = oracle.rope_with_sin_cos_cache(case.positions, case.query, case.key, case.cache, hs, neox,
+                                                     section, cache_mode=cache_mode)
+    assert skipped == 0
+    what = "case %d: %s T=%d hq=%d hk=%d hs=%d R=%d %s section %s mode %d" % (
+        i, dt, T, hq, hk, hs, r, "neox" if neox else "gptj", section, cache_mode)
+    assert_matches(q.cpu(), qo, what + " query")
+    assert_matches(k.cpu(), ko, what + " key")
+    assert R.get_device_error() == 0
