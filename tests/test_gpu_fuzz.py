@@ -1,6 +1,8 @@
 """Seeded random parity sweep: shapes, dtypes, slices, cos/sin layouts, modes
-and directions of the in-place operator, and head sizes, rotary dims, styles,
-mrope sections and splices of the cache operator, each case checked against
+and directions of the in-place operator; head sizes, rotary dims, styles,
+mrope sections and splices of the cache operator; head counts, head sizes,
+batch compositions, block sizes and padding of the fused QKV operator; each
+case checked against
 the oracle with the tolerances of ``parity.py``.  The cases are drawn from a
 fixed seed per case, so a failure names a reproducible case."""
 import numpy as np
@@ -86,3 +88,25 @@ def test_cache_random_case(rope_gpu, i):
     assert_matches(q.cpu(), qo, what + " query")
     assert_matches(k.cpu(), ko, what + " key")
     assert R.get_device_error() == 0
+
+
+@pytest.mark.parametrize("i", range(50))
+def test_fused_qkv_random_case(rope_gpu, i):
+    from test_gpu_qkv import _check, _run_gpu, _run_oracle
+    rng = np.random.default_rng(9000 + i)
+    dt = [torch.float32, torch.float16, torch.bfloat16][rng.integers(3)]
+    mult, top = (16, 256) if dt == torch.float32 else (32, 512)
+    D = mult * int(rng.integers(1, top // mult + 1))
+    nq, nk, nv = int(rng.integers(0, 9)), int(rng.integers(0, 5)), int(rng.integers(0, 5))
+    if nq + nk + nv == 0:
+        nq = 1
+    B = int(rng.integers(1, 12))
+    qlens = [int(v) for v in rng.integers(0, 40, B)]
+    if sum(qlens) == 0:
+        qlens[0] = 1
+    ctx = [int(v) for v in rng.integers(0, 300, B)]
+    bs = int(rng.choice([1, 4, 16, 32]))
+    pad = int(rng.choice([0, 0, 3, 7]))
+    case = W.qkv_case("fuzz_qkv%d" % i, 9000 + i, qlens, ctx, nq, nk, nv, D, bs, dt, pad_every=pad)
+    bp, bslot = _check(case, _run_gpu(case), _run_oracle(case))
+    assert bp == 0 and bslot == 0 and R.get_device_error() == 0
