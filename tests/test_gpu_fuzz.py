@@ -2,9 +2,9 @@
 and directions of the in-place operator; head sizes, rotary dims, styles,
 mrope sections and splices of the cache operator; head counts, head sizes,
 batch compositions, block sizes and padding of the fused QKV operator; each
-case checked against
-the oracle with the tolerances of ``parity.py``.  The cases are drawn from a
-fixed seed per case, so a failure names a reproducible case."""
+case checked against the oracle with the tolerances of the parity tests.  The
+cases are drawn from a fixed seed per case, so a failure names a reproducible
+case."""
 import numpy as np
 import pytest
 import torch
