@@ -1,6 +1,7 @@
 """Seeded random parity sweep: shapes, dtypes, slices, cos/sin layouts, modes
 and directions of the in-place operator; head sizes, rotary dims, styles,
-mrope sections and splices of the cache operator; head counts, head sizes,
+mrope sections and splices of the cache operator, with V2 row views and
+separate outputs; head counts, head sizes,
 batch compositions, block sizes and padding of the fused QKV operator; each
 case checked against the oracle with the tolerances of the parity tests.  The
 cases are drawn from a fixed seed per case, so a failure names a reproducible
@@ -110,3 +111,46 @@ def test_fused_qkv_random_case(rope_gpu, i):
     case = W.qkv_case("fuzz_qkv%d" % i, 9000 + i, qlens, ctx, nq, nk, nv, D, bs, dt, pad_every=pad)
     bp, bslot = _check(case, _run_gpu(case), _run_oracle(case))
     assert bp == 0 and bslot == 0 and R.get_device_error() == 0
+
+
+@pytest.mark.parametrize("i", range(50))
+def test_cache_v2_random_case(rope_gpu, i):
+    """V2: query and key as row views of a wider buffer (extra columns between
+    and after them), optionally written to separate whole-row outputs."""
+    rng = np.random.default_rng(9500 + i)
+    dt = [torch.float32, torch.float16, torch.bfloat16][rng.integers(3)]
+    mult = 16 if dt == torch.float32 else 32
+    hs = mult * int(rng.integers(1, 256 // mult + 1))
+    r = mult * int(rng.integers(1, hs // mult + 1))
+    T, hq, hk = int(rng.integers(1, 200)), int(rng.integers(1, 6)), int(rng.integers(1, 4))
+    neox = bool(rng.integers(0, 2))
+    section = None
+    if rng.random() < 0.4 and r >= 8:
+        a = int(rng.integers(1, r // 2 - 1)) if r // 2 > 2 else 1
+        b = int(rng.integers(0, r // 2 - a + 1))
+        section = [a, b, r // 2 - a - b]
+    case = W.cache_case("fuzz_v2_%d" % i, 9500 + i, T, hq, hk, hs, r, int(rng.integers(1, 2000)), dt, neox,
+                        mrope_section=section)
+    wq, wk = hq * hs, hk * hs
+    gap = hs * int(rng.integers(0, 3))  # extra heads between q and k and after k
+    buf = torch.zeros(T, wq + gap + wk + gap, dtype=dt, device="cuda")
+    buf[:, :wq].copy_(case.query.cuda())
+    buf[:, wq + gap:wq + gap + wk].copy_(case.key.cuda())
+    q, k = buf[:, :wq], buf[:, wq + gap:wq + gap + wk]
+    out = bool(rng.integers(0, 2))
+    qo = torch.full((T, wq), 9.0, dtype=dt, device="cuda") if out else None
+    ko = torch.full((T, wk), 9.0, dtype=dt, device="cuda") if out else None
+    R.rope_with_sin_cos_cache(case.positions.cuda(), q, k, case.cache.cuda(), hs, r, neox, section,
+                              query_out=qo, key_out=ko)
+    torch.cuda.synchronize()
+    ref_q, ref_k, skipped = oracle.rope_with_sin_cos_cache(case.positions, case.query, case.key, case.cache, hs,
+                                                           neox, section)
+    assert skipped == 0
+    what = "case %d: %s T=%d hs=%d R=%d %s section %s gap %d out %s" % (
+        i, dt, T, hs, r, "neox" if neox else "gptj", section, gap, out)
+    got_q, got_k = (qo, ko) if out else (q, k)
+    assert_matches(got_q.cpu(), ref_q, what + " query")
+    assert_matches(got_k.cpu(), ref_k, what + " key")
+    if out:  # inputs untouched
+        assert torch.equal(q.cpu(), case.query) and torch.equal(k.cpu(), case.key)
+    assert R.get_device_error() == 0
