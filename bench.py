@@ -695,7 +695,7 @@ def run_size_sweep(args):
         return W.qkv_case("qkv_%dtok" % (4 * int(1984 * f) + 256), 5, [int(1984 * f)] * 4 + [1] * 256,
                           [4096] * 4 + ctx, 32, 8, 8, 128, 16, torch.bfloat16)
 
-    def factory(c):
+    def factory(c, mode=1, backward=False, cache_mode=0, out_of_place=False, views=False):
         if hasattr(c, "qkv"):
             ro = [t.to(dev) for t in (c.q_gamma, c.k_gamma, c.cache, c.seq_lens, c.query_start_loc, c.slot_mapping)]
             ts = [t.to(dev) for t in (c.qkv, c.q_out, c.k_cache, c.v_cache)]
@@ -705,24 +705,46 @@ def run_size_sweep(args):
         if hasattr(c, "x"):
             cs, sn = c.cos.to(dev), c.sin.to(dev)
             x = c.x.to(dev)
-            return lambda n: [R.prepare_inplace_partial(t[0], cs, sn, 1, [c.start, c.end]) for t in copies(x, n=n)]
+            return lambda n: [R.prepare_inplace_partial(t[0], cs, sn, mode, [c.start, c.end], backward=backward)
+                              for t in copies(x, n=n)]
         p, cc = c.positions.to(dev), c.cache.to(dev)
         q, k = c.query.to(dev), c.key.to(dev)
+        if out_of_place:
+            return lambda n: [R.prepare_with_sin_cos_cache(p, t[0], t[1], cc, c.head_size, c.rotary_dim, c.is_neox,
+                                                           c.mrope_section, query_out=t[2], key_out=t[3])
+                              for t in copies(q, k, torch.empty_like(q), torch.empty_like(k), n=n)]
+        if views:  # q and k as row views of a fused [T, q | k | k-sized v] buffer
+            wq, wk = q.shape[1], k.shape[1]
+            buf = torch.empty(q.shape[0], wq + 2 * wk, dtype=q.dtype, device=dev)
+            buf[:, :wq].copy_(q)
+            buf[:, wq:wq + wk].copy_(k)
+            return lambda n: [R.prepare_with_sin_cos_cache(p, t[0][:, :wq], t[0][:, wq:wq + wk], cc, c.head_size,
+                                                           c.rotary_dim, c.is_neox, c.mrope_section)
+                              for t in copies(buf, n=n)]
         return lambda n: [R.prepare_with_sin_cos_cache(p, t[0], t[1], cc, c.head_size, c.rotary_dim, c.is_neox,
-                                                       c.mrope_section) for t in copies(q, k, n=n)]
+                                                       c.mrope_section, cache_mode=cache_mode)
+                          for t in copies(q, k, n=n)]
 
-    families = [("inplace_bf16x_f32cs_Bx4096x32x128_slice64_128", lambda f: W.inplace_bf16_mixed(int(4 * f))),
-                ("rope_neox_bf16_32q8k_h128", lambda f: W.cache_neox_bf16(int(16384 * f))),
-                ("rope_gptj_f16_16q16k_h256_r64", lambda f: W.cache_gptj_f16_partial(int(8 * f))),
-                ("mrope_neox_bf16_28q4k_h128_s16_24_24", mrope),
-                ("qkv_rmsnorm_rope_bf16_32q8k8v_h128", qkv)]
+    inplace = lambda f: W.inplace_bf16_mixed(int(4 * f))  # noqa: E731
+    neox = lambda f: W.cache_neox_bf16(int(16384 * f))  # noqa: E731
+    gptj = lambda f: W.cache_gptj_f16_partial(int(8 * f))  # noqa: E731
+    families = [("inplace_bf16x_f32cs_Bx4096x32x128_slice64_128", inplace, {}),
+                ("rope_neox_bf16_32q8k_h128", neox, {}),
+                ("rope_gptj_f16_16q16k_h256_r64", gptj, {}),
+                ("mrope_neox_bf16_28q4k_h128_s16_24_24", mrope, {}),
+                ("qkv_rmsnorm_rope_bf16_32q8k8v_h128", qkv, {}),
+                ("inplace_backward_interleave_bf16x_f32cs", inplace, {"backward": True}),
+                ("inplace_half_forward_bf16x_f32cs", inplace, {"mode": 0}),
+                ("mrope_interleaved_splice_neox_bf16", mrope, {"cache_mode": 1}),
+                ("rope_neox_out_of_place_bf16", neox, {"out_of_place": True}),
+                ("rope_gptj_fused_qkv_views_f16", gptj, {"views": True})]
     out = []
-    for name, make in families:
+    for name, make, opts in families:
         pts = []
         for f in (0.5, 1.0, 1.5, 2.0):
             c = make(f)
             nbytes = algorithmic_bytes(c)
-            us, _ = stream_us(factory(c), nbytes)
+            us, _ = stream_us(factory(c, **opts), nbytes)
             pts.append({"tokens": c.tokens, "bytes": nbytes, "us": round(us, 3)})
             del c
             torch.cuda.empty_cache()
