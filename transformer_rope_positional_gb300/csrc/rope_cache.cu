@@ -15,9 +15,11 @@
 // neighbouring pairs) and the matching cos/sin elements, gathered once per
 // item (mrope: spliced from the section rows) and kept in registers for its U
 // rows.  All U row loads are issued before the gather and any arithmetic, so
-// each thread keeps U (NeoX: 2U) 16-byte streaming reads in flight.  q/k are read and written once with evict-first
-// accesses; the cache goes through the read-only path and stays in L2.
-// Columns [R, head_size) of every head are never touched.
+// each thread keeps U (NeoX: 2U) 16-byte streaming reads in flight; the
+// in-place NeoX variants also load the next item's position rows early, so
+// their gather leaves with the row loads.  q/k are read and written once with
+// evict-first accesses; the cache goes through the read-only path and stays
+// in L2.  Columns [R, head_size) of every head are never touched.
 //
 // A position outside [0, maxSeqLen) leaves its token untouched and sets bit
 // ROPE_DEVICE_POSITION_OUT_OF_RANGE of the device error word below.
