@@ -36,7 +36,9 @@ def shard_cache_inputs(positions: torch.Tensor, query: torch.Tensor, key: torch.
 def shard_inplace_inputs(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rank: int, world: int):
     """This rank's part of the in-place operator's inputs: x [B, S, N, D] is cut
     along B when B >= world, else along S; cos/sin follow the cut on the dims
-    they do not broadcast."""
+    they do not broadcast.  A cut along S with B > 1 is a strided view: move it
+    to the rank's device with ``.contiguous()`` (the operator takes contiguous
+    tensors) and gather the results back the same way."""
     B, S = x.shape[0], x.shape[1]
     if B >= world:
         a, b = token_range(B, rank, world)
