@@ -690,9 +690,10 @@ def run_size_sweep(args):
         return W.cache_case("mrope_%dtok" % pos.shape[1], 4, pos.shape[1], 28, 4, 128, 128, 40960, torch.bfloat16,
                             True, base=1e6, positions=pos, mrope_section=[16, 24, 24])
 
-    def qkv(f):
-        ctx = W.uniform_int(W.stream_seed(5, 3), 256, 16, 1024).tolist()
-        return W.qkv_case("qkv_%dtok" % (4 * int(1984 * f) + 256), 5, [int(1984 * f)] * 4 + [1] * 256,
+    def qkv(f):  # the prefill chunks and the number of decode requests both scale
+        nd = int(256 * f)
+        ctx = W.uniform_int(W.stream_seed(5, 3), nd, 16, 1024).tolist()
+        return W.qkv_case("qkv_%dtok" % (4 * int(1984 * f) + nd), 5, [int(1984 * f)] * 4 + [1] * nd,
                           [4096] * 4 + ctx, 32, 8, 8, 128, 16, torch.bfloat16)
 
     def factory(c, mode=1, backward=False, cache_mode=0, out_of_place=False, views=False):
