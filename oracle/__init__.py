@@ -189,6 +189,8 @@ def qkv_rmsnorm_rope_cache(qkv: torch.Tensor, num_q_heads: int, num_k_heads: int
         x.data_ptr(), _CODE[x.dtype], T, num_q_heads, num_k_heads, num_v_heads, D, qg.data_ptr(), kg.data_ptr(),
         float(eps), c.data_ptr(), c.shape[0], sl.data_ptr(), qs.data_ptr(), sl.shape[0], sm.data_ptr(),
         kc.shape[2], kc.shape[0], qo.data_ptr(), kc.data_ptr(), vc.data_ptr())
+    if r == -2:
+        raise ValueError("query_start_loc must be non-decreasing within [0, T]")
     if r < 0:
         raise MemoryError("oracle allocation failed")
     return qo, kc, vc, int(r & 0xFFFFFFFF), int(r >> 32)

@@ -378,6 +378,9 @@ int64_t oracle_qkv_rmsnorm_rope_cache(const void* qkv, int dt, int64_t T, int64_
                                       int64_t block_size, int64_t num_blocks, void* q_out, void* k_cache,
                                       void* v_cache) {
   const int64_t W = (nq + nk + nv) * D, half = D / 2;
+  /* tokens of batch b are [qsl[b], qsl[b+1]): qsl must be non-decreasing inside [0, T] */
+  for (int64_t b = 0; b <= B; ++b)
+    if (qsl[b] < 0 || qsl[b] > T || (b > 0 && qsl[b] < qsl[b - 1])) return -2;
   double* x = (double*)malloc(sizeof(double) * (size_t)D);
   double* y = (double*)malloc(sizeof(double) * (size_t)D);
   double* o = (double*)malloc(sizeof(double) * (size_t)D);

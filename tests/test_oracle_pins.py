@@ -736,3 +736,13 @@ def test_qkv_bad_position_and_slot_are_skipped():
     assert bp == 1 and bs == 1
     assert _same_bits(qo[3], case.q_out[3])  # bad position: q row unwritten
     assert not _same_bits(qo[0], case.q_out[0])  # bad slot: q still computed
+
+
+def test_qkv_oracle_rejects_malformed_query_start_loc():
+    """Batch b's tokens are [qsl[b], qsl[b+1]) ([QKV] §计算公式): a decreasing
+    queryStartLoc, or one outside [0, T], is refused rather than read past."""
+    c = W.qkv_case("bad_qsl", 3, [3, 2], [0, 4], 2, 1, 1, 64, 4, torch.float16)
+    for bad in ([0, 4, 2], [0, 2, 6], [-1, 2, 5]):
+        with pytest.raises(ValueError):
+            oracle.qkv_rmsnorm_rope_cache(c.qkv, 2, 1, 1, c.q_gamma, c.k_gamma, c.eps, c.cache, c.seq_lens,
+                                          torch.tensor(bad), c.slot_mapping, c.q_out, c.k_cache, c.v_cache)
