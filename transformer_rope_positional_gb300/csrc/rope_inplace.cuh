@@ -195,11 +195,11 @@ __global__ void __launch_bounds__(256) inplace_pair_kernel(TX* __restrict__ x, c
   wait_for_prior_grid();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / pairs;
+    const int64_t r = div_index(i, pairs, a.items32);
     const int64_t q = i - r * pairs;
-    const int64_t n = r % a.N;
-    const int64_t token = r / a.N;
-    const int64_t b = token / a.S;
+    const int64_t token = div_index(r, a.N, a.items32);
+    const int64_t n = r - token * a.N;
+    const int64_t b = div_index(token, a.S, a.items32);
     const int64_t s = token - b * a.S;
     const int64_t j = HALF ? q : 2 * q;           // slot
     const int64_t j2 = HALF ? q + pairs : 2 * q + 1;  // partner
@@ -259,6 +259,7 @@ cudaError_t launch_pairs(const InplaceProblem& p, cudaStream_t stream) {
   InplaceArgs a = base_args(p);
   const int64_t rows = p.B * p.S * p.N;
   const int64_t total = rows * (p.L / 2);
+  a.items32 = total <= 0xffffffffLL;  // pair indices (and so rows and tokens) fit 32 bits
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)sm_count() * 8);
   return launch_overlapped(inplace_pair_kernel<TX, TC, HALF, BWD>, (unsigned)std::max<int64_t>(1, blocks), 256,
                            stream, static_cast<TX*>(p.x), static_cast<const TC*>(p.cos),
