@@ -1,0 +1,73 @@
+"""Host-side pieces of bench.py: the byte model behind every GB/s figure, the
+CPU-baseline samples and the recorded-traffic lookup (no GPU needed)."""
+import os
+
+import pytest
+import torch
+
+import bench
+import workloads as W
+
+
+def test_byte_model_of_the_hot_path_workloads():
+    """Read + write of the rotated elements, plus cos/sin (or one gathered cache
+    row per token) and the positions, worked out from the shapes by hand."""
+    inplace, neox, gptj, mrope = bench.build_workloads()
+    # x bf16 [4,4096,32,128], slice of 64: read+write; cos/sin f32 [1,4096,1,64] read
+    assert bench.algorithmic_bytes(inplace) == 4 * 4096 * 32 * 64 * 2 * 2 + 2 * 4096 * 64 * 4 == 136314880
+    # q 32 + k 8 heads of 128 bf16 read+write per token, one 128-wide cache row, one int64 position
+    assert bench.algorithmic_bytes(neox) == 16384 * (40 * 128 * 2 * 2 + 128 * 2 + 8) == 339869696
+    # 16 + 16 heads, only R = 64 of 256 columns touched, f16
+    assert bench.algorithmic_bytes(gptj) == 8192 * (32 * 64 * 2 * 2 + 64 * 2 + 8) == 68222976
+    # 28 + 4 heads of 128 bf16, one cache row-equivalent, three int64 positions
+    assert bench.algorithmic_bytes(mrope) == 32768 * (32 * 128 * 2 * 2 + 128 * 2 + 3 * 8) == 546045952
+    small = W.inplace_f32_small("slice")  # x f32 [1,16,2,64], slice [16,48): 32 columns
+    assert bench.algorithmic_bytes(small) == 16 * 2 * 32 * 4 * 2 + 2 * 16 * 32 * 4 == 12288
+
+
+def test_byte_model_of_the_fused_op():
+    c = W.qkv_case("bytes", 1, [5, 1, 3], [0, 7, 20], 4, 2, 2, 64, 4, torch.bfloat16, pad_every=4)
+    T, D, e = 9, 64, 2
+    cached = int((c.slot_mapping >= 0).sum())
+    assert cached < T  # padding slots write no cache rows
+    want = (T * 8 * D * e            # qkv read
+            + T * 4 * D * e          # q_out written
+            + cached * 4 * D * e     # k and v rows cached
+            + T * D * e              # one cos/sin row per token
+            + 2 * D * e              # the two gammas
+            + (3 + 4 + 9) * 8)       # seqLens, queryStartLoc, slotMapping
+    assert bench.algorithmic_bytes(c) == want
+
+
+def test_cpu_samples_cover_whole_batches_and_prefixes():
+    inplace, neox, gptj, mrope = bench.build_workloads()
+    whole = bench.oracle_sample(inplace, inplace.tokens)
+    assert tuple(whole.x.shape) == (4, 4096, 32, 128)
+    assert bench.algorithmic_bytes(whole) == bench.algorithmic_bytes(inplace)
+    assert tuple(bench.oracle_sample(inplace, 5000).x.shape) == (1, 4096, 32, 128)
+    part = bench.oracle_sample(inplace, 300)
+    assert tuple(part.x.shape) == (1, 300, 32, 128) and tuple(part.cos.shape) == (1, 300, 1, 64)
+    m = bench.oracle_sample(mrope, 1000)
+    assert m.tokens == 1000 and tuple(m.positions.shape) == (3, 1000)
+    assert torch.equal(m.query, mrope.query[:1000])
+
+
+def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    label = "mrope_neox_bf16_32768tok_28q4k_h128_s16_24_24"
+    (tmp_path / "profiles").mkdir()
+    table = tmp_path / "profiles" / "dram_traffic.txt"
+    table.write_text("kernel_source_sha256_16: %s\n%s: 123456\n" % (bench.kernel_source_hash(), label))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "f" * 16)
+    assert bench.recorded_traffic(label) is None  # sources changed since the capture
+    table.write_text("kernel_source_sha256_16: %s\n%s: 123456\n" % ("f" * 16, label))
+    assert bench.recorded_traffic(label) == 123456
+    assert bench.recorded_traffic("unknown_label") is None
+
+
+def test_committed_traffic_table_matches_the_sources():
+    """profiles/dram_traffic.txt was captured on the kernel sources as committed."""
+    path = os.path.join(os.path.dirname(bench.__file__), "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        pytest.skip("no traffic table")
+    assert bench.recorded_traffic("mrope_neox_bf16_32768tok_28q4k_h128_s16_24_24") is not None
