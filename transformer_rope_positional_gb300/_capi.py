@@ -148,6 +148,24 @@ def _slice(partial_slice):
     return int(partial_slice[0]), int(partial_slice[1])
 
 
+def _inplace_args(x, cos, sin, rotary_mode, partial_slice, stream, backward):
+    """(C function, its arguments, objects to keep alive, name) of one call."""
+    lib = load()
+    start, end = _slice(partial_slice)
+    dx, dc, ds = tensor_desc(x), tensor_desc(cos), tensor_desc(sin)
+    args = (ctypes.byref(dx), ctypes.byref(dc), ctypes.byref(ds), _mode(rotary_mode), start, end,
+            _stream_handle(x, stream))
+    if backward:
+        return lib.rope_inplace_partial_backward, args, (x, cos, sin, dx, dc, ds), "rope_inplace_partial_backward"
+    return lib.rope_inplace_partial, args, (x, cos, sin, dx, dc, ds), "rope_inplace_partial"
+
+
+def _run(fn, args, what) -> None:
+    st = fn(*args)
+    if st != ROPE_OK:
+        raise RopeError(st, what)
+
+
 def rope_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode=1,
                          partial_slice: Optional[Sequence[int]] = None, stream=None) -> None:
     """In-place partial RoPE of ``x`` [B, S, N, D] over ``partial_slice``.
@@ -156,26 +174,16 @@ def rope_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, 
     means ``[0, 0]``, the whole D axis.  Returns None; x is rewritten on
     ``stream`` (default: the current stream of x's device).
     """
-    start, end = _slice(partial_slice)
-    lib = load()
-    dx, dc, ds = tensor_desc(x), tensor_desc(cos), tensor_desc(sin)
-    st = lib.rope_inplace_partial(ctypes.byref(dx), ctypes.byref(dc), ctypes.byref(ds), _mode(rotary_mode),
-                                  start, end, _stream_handle(x, stream))
-    if st != ROPE_OK:
-        raise RopeError(st, "rope_inplace_partial")
+    fn, args, _, what = _inplace_args(x, cos, sin, rotary_mode, partial_slice, stream, False)
+    _run(fn, args, what)
 
 
 def rope_inplace_partial_backward(grad: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode=1,
                                   partial_slice: Optional[Sequence[int]] = None, stream=None) -> None:
     """Backward of :func:`rope_inplace_partial`: turns dL/dy in ``grad`` into
     dL/dx in place."""
-    start, end = _slice(partial_slice)
-    lib = load()
-    dg, dc, ds = tensor_desc(grad), tensor_desc(cos), tensor_desc(sin)
-    st = lib.rope_inplace_partial_backward(ctypes.byref(dg), ctypes.byref(dc), ctypes.byref(ds),
-                                           _mode(rotary_mode), start, end, _stream_handle(grad, stream))
-    if st != ROPE_OK:
-        raise RopeError(st, "rope_inplace_partial_backward")
+    fn, args, _, what = _inplace_args(grad, cos, sin, rotary_mode, partial_slice, stream, True)
+    _run(fn, args, what)
 
 
 def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: torch.Tensor,
@@ -189,6 +197,16 @@ def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: t
     be strided row views (e.g. slices of a fused QKV tensor); ``cache_mode=1``
     selects the interleaved mrope splice.  Contiguous in-place calls with
     ``cache_mode=0`` use the V1 entry point, everything else the V2 one."""
+    fn, args, _, what = _cache_args(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_neox,
+                                    mrope_section, stream, cache_mode, query_out, key_out)
+    _run(fn, args, what)
+
+
+def _cache_args(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_neox, mrope_section, stream,
+                cache_mode, query_out, key_out):
+    """(C function, its arguments, objects to keep alive, name) of one
+    cache-operator call: the V1 entry point for a contiguous in-place call with
+    cache_mode 0, else V2."""
     lib = load()
     R = int(cos_sin_cache.shape[1]) if rotary_dim is None else int(rotary_dim)
     dp, dc = tensor_desc(positions), tensor_desc(cos_sin_cache)
@@ -202,19 +220,18 @@ def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: t
     handle = _stream_handle(query, stream)
     contiguous = qs == query.shape[1] and ks == key.shape[1]
     if cache_mode == 0 and query_out is None and key_out is None and contiguous:
-        st = lib.rope_with_sin_cos_cache(ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc),
-                                         int(head_size), R, 1 if is_neox else 0, sec, n_sec, handle)
-        what = "rope_with_sin_cos_cache"
-    else:
-        dqo = tensor_desc(query_out) if query_out is not None else None
-        dko = tensor_desc(key_out) if key_out is not None else None
-        st = lib.rope_with_sin_cos_cache_v2(ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc),
-                                            int(head_size), R, 1 if is_neox else 0, sec, n_sec, int(cache_mode),
-                                            qs, ks, ctypes.byref(dqo) if dqo is not None else None,
-                                            ctypes.byref(dko) if dko is not None else None, handle)
-        what = "rope_with_sin_cos_cache_v2"
-    if st != ROPE_OK:
-        raise RopeError(st, what)
+        args = (ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc), int(head_size), R,
+                1 if is_neox else 0, sec, n_sec, handle)
+        return (lib.rope_with_sin_cos_cache, args, (positions, query, key, cos_sin_cache, dp, dq, dk, dc, sec),
+                "rope_with_sin_cos_cache")
+    dqo = tensor_desc(query_out) if query_out is not None else None
+    dko = tensor_desc(key_out) if key_out is not None else None
+    args = (ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc), int(head_size), R,
+            1 if is_neox else 0, sec, n_sec, int(cache_mode), qs, ks,
+            ctypes.byref(dqo) if dqo is not None else None, ctypes.byref(dko) if dko is not None else None, handle)
+    return (lib.rope_with_sin_cos_cache_v2, args,
+            (positions, query, key, cos_sin_cache, query_out, key_out, dp, dq, dk, dc, dqo, dko, sec),
+            "rope_with_sin_cos_cache_v2")
 
 
 def _qkv_args(qkv, num_q_heads, num_k_heads, num_v_heads, q_gamma, k_gamma, eps, cos_sin_cache, seq_lens,
@@ -235,9 +252,7 @@ def qkv_rmsnorm_rope_cache(qkv: torch.Tensor, num_q_heads: int, num_k_heads: int
     lib = load()
     args, _ = _qkv_args(qkv, num_q_heads, num_k_heads, num_v_heads, q_gamma, k_gamma, eps, cos_sin_cache,
                         seq_lens, query_start_loc, slot_mapping, q_out, k_cache, v_cache, stream)
-    st = lib.rope_qkv_rmsnorm_rope_cache(*args)
-    if st != ROPE_OK:
-        raise RopeError(st, "rope_qkv_rmsnorm_rope_cache")
+    _run(lib.rope_qkv_rmsnorm_rope_cache, args, "rope_qkv_rmsnorm_rope_cache")
 
 
 def prepare_qkv_rmsnorm_rope_cache(qkv: torch.Tensor, num_q_heads: int, num_k_heads: int, num_v_heads: int,
@@ -294,14 +309,8 @@ class PreparedCall:
 def prepare_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode=1,
                             partial_slice: Optional[Sequence[int]] = None, stream=None,
                             backward: bool = False) -> PreparedCall:
-    lib = load()
-    start, end = _slice(partial_slice)
-    dx, dc, ds = tensor_desc(x), tensor_desc(cos), tensor_desc(sin)
-    args = (ctypes.byref(dx), ctypes.byref(dc), ctypes.byref(ds), _mode(rotary_mode), start, end,
-            _stream_handle(x, stream))
-    fn = lib.rope_inplace_partial_backward if backward else lib.rope_inplace_partial
-    return PreparedCall(fn, args, (x, cos, sin, dx, dc, ds),
-                        "rope_inplace_partial_backward" if backward else "rope_inplace_partial")
+    """:func:`rope_inplace_partial` (or its backward) with its arguments marshalled once."""
+    return PreparedCall(*_inplace_args(x, cos, sin, rotary_mode, partial_slice, stream, backward))
 
 
 def prepare_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: torch.Tensor,
@@ -309,30 +318,6 @@ def prepare_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key
                                is_neox: bool = True, mrope_section: Optional[Sequence[int]] = None,
                                stream=None, *, cache_mode: int = 0, query_out: Optional[torch.Tensor] = None,
                                key_out: Optional[torch.Tensor] = None) -> PreparedCall:
-    """Marshal one cache-operator call once (V1 entry point when the call is a
-    contiguous in-place one with cache_mode 0, else V2)."""
-    lib = load()
-    R = int(cos_sin_cache.shape[1]) if rotary_dim is None else int(rotary_dim)
-    dp, dc = tensor_desc(positions), tensor_desc(cos_sin_cache)
-    dq, qs = rows_desc(query)
-    dk, ks = rows_desc(key)
-    sec = None
-    n_sec = 0
-    if mrope_section is not None:
-        n_sec = len(mrope_section)
-        sec = (ctypes.c_int64 * max(1, n_sec))(*[int(v) for v in mrope_section])
-    handle = _stream_handle(query, stream)
-    contiguous = qs == query.shape[1] and ks == key.shape[1]
-    if cache_mode == 0 and query_out is None and key_out is None and contiguous:
-        args = (ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc), int(head_size), R,
-                1 if is_neox else 0, sec, n_sec, handle)
-        return PreparedCall(lib.rope_with_sin_cos_cache, args,
-                            (positions, query, key, cos_sin_cache, dp, dq, dk, dc, sec), "rope_with_sin_cos_cache")
-    dqo = tensor_desc(query_out) if query_out is not None else None
-    dko = tensor_desc(key_out) if key_out is not None else None
-    args = (ctypes.byref(dp), ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dc), int(head_size), R,
-            1 if is_neox else 0, sec, n_sec, int(cache_mode), qs, ks,
-            ctypes.byref(dqo) if dqo is not None else None, ctypes.byref(dko) if dko is not None else None, handle)
-    return PreparedCall(lib.rope_with_sin_cos_cache_v2, args,
-                        (positions, query, key, cos_sin_cache, query_out, key_out, dp, dq, dk, dc, dqo, dko, sec),
-                        "rope_with_sin_cos_cache_v2")
+    """:func:`rope_with_sin_cos_cache` with its arguments marshalled once."""
+    return PreparedCall(*_cache_args(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_neox,
+                                     mrope_section, stream, cache_mode, query_out, key_out))
