@@ -94,3 +94,20 @@ def test_mixed_bf16_workload_full_size_other_modes(rope_gpu, run):
                                                 case.start, case.end, rotary_mode=R._capi.MODES[mode],
                                                 backward=backward)
         assert_matches(got[b:b + 1, s:s + 1], ref, "token %d" % t)
+
+
+def test_unaligned_slice_full_size(rope_gpu):
+    """The [4,4096,32,128] bf16 workload with the slice [4,68): 8-byte vectors,
+    and a slice that crosses a 128-byte line of every row."""
+    full = W.inplace_bf16_mixed()
+    case = W.inplace_case("inplace_bf16x_f32cs_4x4096x32x128_slice4_68", 1, tuple(full.x.shape), 4, 68,
+                          torch.bfloat16, torch.float32)
+    got = gpu_inplace(case)
+    assert R.get_device_error() == 0
+    assert same_bits(got[..., :4], case.x[..., :4]) and same_bits(got[..., 68:], case.x[..., 68:])
+    B, S, N, D = case.x.shape
+    for t in _sample(B * S, 106).tolist():
+        b, s = divmod(t, S)
+        ref = oracle.inplace_partial_rotary_mul(case.x[b:b + 1, s:s + 1].contiguous(), case.cos[:, s:s + 1],
+                                                case.sin[:, s:s + 1], 4, 68)
+        assert_matches(got[b:b + 1, s:s + 1], ref, "token %d" % t)
