@@ -111,3 +111,20 @@ def test_unaligned_slice_full_size(rope_gpu):
         ref = oracle.inplace_partial_rotary_mul(case.x[b:b + 1, s:s + 1].contiguous(), case.cos[:, s:s + 1],
                                                 case.sin[:, s:s + 1], 4, 68)
         assert_matches(got[b:b + 1, s:s + 1], ref, "token %d" % t)
+
+
+def test_mrope_interleaved_splice_full_size(rope_gpu):
+    """The mrope workload through the V2 interleaved splice (cacheMode 1)."""
+    case = W.mrope_neox_bf16()
+    q, k = case.query.cuda(), case.key.cuda()
+    R.rope_with_sin_cos_cache(case.positions.cuda(), q, k, case.cache.cuda(), case.head_size, case.rotary_dim,
+                              case.is_neox, case.mrope_section, cache_mode=1)
+    torch.cuda.synchronize()
+    assert R.get_device_error() == 0
+    tok = _sample(case.tokens, 107)
+    qo, ko, skipped = oracle.rope_with_sin_cos_cache(case.positions[..., tok].contiguous(), case.query[tok],
+                                                     case.key[tok], case.cache, case.head_size, case.is_neox,
+                                                     case.mrope_section, cache_mode=1)
+    assert skipped == 0
+    assert_matches(q[tok.cuda()].cpu(), qo, "interleaved splice query")
+    assert_matches(k[tok.cuda()].cpu(), ko, "interleaved splice key")
