@@ -746,3 +746,15 @@ def test_qkv_oracle_rejects_malformed_query_start_loc():
         with pytest.raises(ValueError):
             oracle.qkv_rmsnorm_rope_cache(c.qkv, 2, 1, 1, c.q_gamma, c.k_gamma, c.eps, c.cache, c.seq_lens,
                                           torch.tensor(bad), c.slot_mapping, c.q_out, c.k_cache, c.v_cache)
+
+
+def test_every_golden_fixture_cites_its_source():
+    """Stored expected values come from the pages: each fixture names the page and
+    section it was worked from, and how."""
+    folder = os.path.join(os.path.dirname(__file__), "golden")
+    names = sorted(f for f in os.listdir(folder) if f.endswith(".json"))
+    assert names
+    for name in names:
+        with open(os.path.join(folder, name)) as f:
+            g = json.load(f)
+        assert isinstance(g.get("source"), str) and len(g["source"]) > 20, name
