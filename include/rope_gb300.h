@@ -18,7 +18,9 @@
  *
  * Memory and ownership.  Every tensor is described by a rope_tensor_t that the
  * caller owns; `data` is a DEVICE pointer to contiguous row-major storage,
- * borrowed for the duration of the call and of the work it enqueues.  The
+ * borrowed for the duration of the call and of the work it enqueues.  All
+ * tensors of a call live on the current device (cudaSetDevice), and `stream`
+ * belongs to it: the launch goes to the current device.  The
  * library allocates nothing, needs no workspace, and never synchronises the
  * stream (except rope_get_device_error, which says so).  The two-phase
  * "GetWorkspaceSize, then execute" interface of the pages collapses to one call
@@ -31,7 +33,9 @@
  * are deterministic and do not depend on the launch shape.
  *
  * Errors.  Every argument check happens on the host before anything is
- * enqueued; a failed check returns a status and enqueues nothing.  Status
+ * enqueued; a failed check returns a status and enqueues nothing.  A shape
+ * whose element count (or a strided view's extent) overflows, or exceeds
+ * INT64_MAX / 8, is ROPE_ERR_PARAM_INVALID.  Status
  * values 161001 and 161002 are the ones [IPRM §返回值与错误码] lists
  * (ACLNN_ERR_PARAM_NULLPTR, ACLNN_ERR_PARAM_INVALID).  A CUDA launch error is
  * returned as ROPE_ERR_CUDA; errors that happen while the work runs surface at
@@ -248,11 +252,14 @@ int rope_qkv_rmsnorm_rope_cache(const rope_tensor_t* qkv, int64_t num_q_heads, i
                                 const rope_tensor_t* v_cache, void* stream);
 
 /*
- * Synchronises `stream`, then reads and clears the device-side error word of the
- * current device.  *code receives ROPE_DEVICE_OK or a bitwise OR of the
- * ROPE_DEVICE_* codes recorded by kernels since the last read (by any stream of
- * this device).  Returns ROPE_OK, ROPE_ERR_PARAM_NULLPTR (code is NULL) or
- * ROPE_ERR_CUDA.
+ * Takes the device-side error word of the current device (an atomic exchange
+ * with zero, enqueued on `stream`), then synchronises `stream`.  *code receives
+ * ROPE_DEVICE_OK or a bitwise OR of the ROPE_DEVICE_* codes recorded since the
+ * previous read.  The word is shared by every stream and every caller of this
+ * process on that device: a read returns (and clears) bits that kernels on other
+ * streams recorded too, and no bit is lost between two reads.  Enqueues one
+ * one-thread kernel (counted by rope_launch_count).  Returns ROPE_OK,
+ * ROPE_ERR_PARAM_NULLPTR (code is NULL) or ROPE_ERR_CUDA.
  */
 int rope_get_device_error(void* stream, int32_t* code);
 

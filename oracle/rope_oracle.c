@@ -416,8 +416,8 @@ int64_t oracle_qkv_rmsnorm_rope_cache(const void* qkv, int dt, int64_t T, int64_
         const void* gamma = h < nq ? q_gamma : k_gamma;
         double ss = 0.0;
         for (int64_t j = 0; j < D; ++j) ss += x[j] * x[j];
-        const double inv = 1.0 / sqrt(ss / (double)D + eps);
-        for (int64_t j = 0; j < D; ++j) y[j] = x[j] * inv * load_elem(gamma, dt, j);
+        const double rms = sqrt(ss / (double)D + eps);
+        for (int64_t j = 0; j < D; ++j) y[j] = x[j] / rms * load_elem(gamma, dt, j);
         /* RoPE: concat(low*cos - high*sin, high*cos + low*sin) */
         for (int64_t j = 0; j < half; ++j) {
           const double c = load_elem(cache, dt, position * D + j);

@@ -98,3 +98,33 @@ def assert_close_scaled(got: torch.Tensor, ref: torch.Tensor, scale: np.ndarray,
     bad = ~(both_nan | (err <= bound))
     assert not bad.any(), "%s: %d elements out of bound, worst excess %g" % (
         what, int(bad.sum()), float(np.nanmax(np.where(bad, err - bound, 0))))
+
+
+def compare_terms(got: torch.Tensor, ref: torch.Tensor, terms: np.ndarray, rel: float = FP32_REL_TOL) -> dict:
+    """Element-wise comparison relative to the terms that form each result.
+
+    For an output o = a*c - b*s (or b*c + a*s) built from values a, b that
+    are themselves computed (e.g. RMS-normalised), ``terms`` is |a*c| + |b*s|
+    in float64; a binary32 evaluation is accurate to a small multiple of
+    2^-24 of that sum, whatever cancellation happens in o.  Bound:
+      float32:          |got - ref| <= rel * terms
+      float16/bfloat16: |got - ref| <= 1 ulp(ref) + rel * terms
+    NaN matches NaN.  Returns the largest |got - ref| / terms, the largest ulp
+    distance, the element count and ``ok``."""
+    g = got.detach().cpu().double().numpy()
+    r = ref.detach().cpu().double().numpy()
+    t = np.broadcast_to(np.asarray(terms, dtype=np.float64), r.shape)
+    both_nan = np.isnan(g) & np.isnan(r)
+    with np.errstate(invalid="ignore"):
+        err = np.where(both_nan, 0.0, np.abs(g - r))
+    err = np.where(np.isnan(err), np.inf, err)
+    bound = rel * t
+    if ref.dtype != torch.float32:
+        bound = bound + ulp_of(ref)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        scaled = np.where(err == 0, 0.0, err / t)
+    ulps = ulp_distance(got, ref)
+    return {"n": int(r.size), "ok": bool((err <= bound).all()),
+            "max_err_over_terms": float(scaled.max()) if scaled.size else 0.0,
+            "max_ulp": int(ulps.max()) if ulps.size else 0,
+            "out_of_bound": int((err > bound).sum())}

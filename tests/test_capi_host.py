@@ -295,3 +295,57 @@ def _qkv(lib, **over):
 ])
 def test_qkv_rejections(lib, over, status):
     assert _qkv(lib, **over) == status
+
+
+def test_overlapping_row_views_are_refused_before_the_library():
+    """A row view whose stride is below its width (one row expanded to many:
+    stride 0) would make the operator read and write every row through the
+    same memory; the binding refuses it before building a descriptor."""
+    one = torch.randn(1, 256)
+    with pytest.raises(ValueError, match="rows overlap"):
+        C.rows_desc(one.expand(16, 256))
+    with pytest.raises(ValueError, match="rows overlap"):
+        C.rows_desc(torch.randn(16, 300).as_strided((16, 256), (128, 1)))
+    # a single row is fine whatever its stride; it reports its width
+    with pytest.raises(ValueError, match="CUDA"):
+        C.rows_desc(one.expand(1, 256))
+    with pytest.raises(ValueError, match="overlap"):
+        C.rope_with_sin_cos_cache(torch.zeros(16, dtype=torch.int64), one.expand(16, 256), torch.randn(16, 256),
+                                  torch.randn(8, 128), 128)
+
+
+class _OnDevice:
+    def __init__(self, index):
+        self.index = index
+
+    def get_device(self):
+        return self.index
+
+
+def test_tensors_on_several_devices_are_refused():
+    assert C._one_device(_OnDevice(1), None, _OnDevice(1)) == 1
+    with pytest.raises(ValueError, match="different devices"):
+        C._one_device(_OnDevice(0), _OnDevice(1))
+    with pytest.raises(ValueError, match="different devices"):
+        C._one_device(torch.empty(1), _OnDevice(0))
+
+
+def test_shapes_whose_element_count_overflows_are_refused(lib):
+    """Element counts are taken with overflow checks: a shape whose product
+    wraps int64 (or passes INT64_MAX / 8) is refused, not launched with a
+    wrapped count."""
+    big = 1 << 40
+    assert _inplace(lib, _d(C.F32, (big, big, 2, 64)), _d(C.F32, (1, 1, 1, 64)), _d(C.F32, (1, 1, 1, 64))) \
+        == C.ROPE_ERR_PARAM_INVALID
+    assert _inplace(lib, _d(C.F32, (1 << 30, 1 << 30, 2, 64)), _d(C.F32, (1, 1, 1, 64)),
+                    _d(C.F32, (1, 1, 1, 64))) == C.ROPE_ERR_PARAM_INVALID  # 2^67 elements
+    p, q, k, c = good()
+    assert _cache(lib, _d(C.I64, (1 << 33,)), _d(C.BF16, (1 << 33, 1 << 33)), _d(C.BF16, (1 << 33, 128)), c) \
+        == C.ROPE_ERR_PARAM_INVALID
+    # a row stride whose extent (T - 1) * stride + width wraps
+    assert _v2(lib, p, q, k, c, qs=1 << 62) == C.ROPE_ERR_PARAM_INVALID
+    assert _v2(lib, p, q, k, c, ks=(1 << 62) + 8) == C.ROPE_ERR_PARAM_INVALID
+    # slots = blocks * block size wraps although the caches hold no heads
+    assert _qkv(lib, nq=4, nk=0, nv=0, qkv=_d(C.BF16, (6, 4 * 64)), qo=_d(C.BF16, (6, 4 * 64)),
+                kc=_d(C.BF16, (big, 0, 1 << 30, 64)), vc=_d(C.BF16, (big, 0, 1 << 30, 64))) \
+        == C.ROPE_ERR_PARAM_INVALID

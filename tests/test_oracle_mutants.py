@@ -54,11 +54,11 @@ MUTANTS = [
      "for (int64_t i = 1; i < 3 * mrope_section[1] && i < half; i += 3) {",
      "for (int64_t i = 0; i < 3 * mrope_section[1] && i < half; i += 3) {"),
     ("fused: mean over D - 1",
-     "const double inv = 1.0 / sqrt(ss / (double)D + eps);",
-     "const double inv = 1.0 / sqrt(ss / (double)(D - 1) + eps);"),
+     "const double rms = sqrt(ss / (double)D + eps);",
+     "const double rms = sqrt(ss / (double)(D - 1) + eps);"),
     ("fused: gamma index shifted",
-     "for (int64_t j = 0; j < D; ++j) y[j] = x[j] * inv * load_elem(gamma, dt, j);",
-     "for (int64_t j = 0; j < D; ++j) y[j] = x[j] * inv * load_elem(gamma, dt, (j + 1) % D);"),
+     "for (int64_t j = 0; j < D; ++j) y[j] = x[j] / rms * load_elem(gamma, dt, j);",
+     "for (int64_t j = 0; j < D; ++j) y[j] = x[j] / rms * load_elem(gamma, dt, (j + 1) % D);"),
     ("fused: q gamma for k",
      "const void* gamma = h < nq ? q_gamma : k_gamma;", "const void* gamma = q_gamma;"),
     ("fused: rope sign",

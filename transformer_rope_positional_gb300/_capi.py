@@ -108,14 +108,46 @@ def tensor_desc(t: torch.Tensor) -> RopeTensor:
 
 def rows_desc(t: torch.Tensor):
     """Describe a 2-D CUDA tensor whose rows may be strided (unit column
-    stride); returns (descriptor, row stride in elements)."""
-    if not t.is_cuda:
-        raise ValueError("expected a CUDA tensor, got one on %s" % t.device)
+    stride); returns (descriptor, row stride in elements).
+
+    Rows must not overlap: a view whose row stride is below its row width
+    (e.g. ``expand`` of one row, stride 0) is refused, since the operator
+    writes every row.  A tensor of at most one row gets its width as stride."""
     if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
         raise ValueError("expected a 2-D tensor with contiguous rows")
+    width = int(t.shape[1])
+    stride = int(t.stride(0)) if t.shape[0] > 1 else width
+    if stride < width:
+        raise ValueError("rows overlap: row stride %d is below the row width %d" % (stride, width))
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor, got one on %s" % t.device)
     if t.dtype not in DTYPE_CODE:
         raise ValueError("unsupported dtype %s" % t.dtype)
-    return describe(t.data_ptr(), DTYPE_CODE[t.dtype], tuple(t.shape)), int(t.stride(0))
+    return describe(t.data_ptr(), DTYPE_CODE[t.dtype], tuple(t.shape)), stride
+
+
+def _one_device(*tensors) -> int:
+    """Index of the CUDA device that holds every given tensor (None entries
+    skipped); raises if they are spread over several devices."""
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        d = t.get_device()
+        if dev is None:
+            dev = d
+        elif d != dev:
+            raise ValueError("tensors on different devices (cuda:%d and cuda:%d)" % (dev, d))
+    return dev
+
+
+def _on_device(dev: int, fn, args):
+    """Call fn(*args) with device ``dev`` current (the library launches on the
+    current device and sizes its grid from it)."""
+    if dev is None or dev < 0 or torch.cuda.current_device() == dev:
+        return fn(*args)
+    with torch.cuda.device(dev):
+        return fn(*args)
 
 
 # the current stream's raw handle without building a Stream object (about 10x
@@ -128,6 +160,8 @@ def _stream_handle(t: torch.Tensor, stream) -> int:
         if _raw_current_stream is not None:
             return _raw_current_stream(t.get_device())
         return torch.cuda.current_stream(t.device).cuda_stream
+    if hasattr(stream, "device") and stream.device.index != t.get_device():
+        raise ValueError("stream of %s for tensors on cuda:%d" % (stream.device, t.get_device()))
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -152,6 +186,7 @@ def _inplace_args(x, cos, sin, rotary_mode, partial_slice, stream, backward):
     """(C function, its arguments, objects to keep alive, name) of one call."""
     lib = load()
     start, end = _slice(partial_slice)
+    _one_device(x, cos, sin)
     dx, dc, ds = tensor_desc(x), tensor_desc(cos), tensor_desc(sin)
     args = (ctypes.byref(dx), ctypes.byref(dc), ctypes.byref(ds), _mode(rotary_mode), start, end,
             _stream_handle(x, stream))
@@ -160,8 +195,8 @@ def _inplace_args(x, cos, sin, rotary_mode, partial_slice, stream, backward):
     return lib.rope_inplace_partial, args, (x, cos, sin, dx, dc, ds), "rope_inplace_partial"
 
 
-def _run(fn, args, what) -> None:
-    st = fn(*args)
+def _run(fn, args, keep, what) -> None:
+    st = _on_device(keep[0].get_device(), fn, args)
     if st != ROPE_OK:
         raise RopeError(st, what)
 
@@ -174,16 +209,14 @@ def rope_inplace_partial(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, 
     means ``[0, 0]``, the whole D axis.  Returns None; x is rewritten on
     ``stream`` (default: the current stream of x's device).
     """
-    fn, args, _, what = _inplace_args(x, cos, sin, rotary_mode, partial_slice, stream, False)
-    _run(fn, args, what)
+    _run(*_inplace_args(x, cos, sin, rotary_mode, partial_slice, stream, False))
 
 
 def rope_inplace_partial_backward(grad: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor, rotary_mode=1,
                                   partial_slice: Optional[Sequence[int]] = None, stream=None) -> None:
     """Backward of :func:`rope_inplace_partial`: turns dL/dy in ``grad`` into
     dL/dx in place."""
-    fn, args, _, what = _inplace_args(grad, cos, sin, rotary_mode, partial_slice, stream, True)
-    _run(fn, args, what)
+    _run(*_inplace_args(grad, cos, sin, rotary_mode, partial_slice, stream, True))
 
 
 def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: torch.Tensor,
@@ -197,9 +230,8 @@ def rope_with_sin_cos_cache(positions: torch.Tensor, query: torch.Tensor, key: t
     be strided row views (e.g. slices of a fused QKV tensor); ``cache_mode=1``
     selects the interleaved mrope splice.  Contiguous in-place calls with
     ``cache_mode=0`` use the V1 entry point, everything else the V2 one."""
-    fn, args, _, what = _cache_args(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_neox,
-                                    mrope_section, stream, cache_mode, query_out, key_out)
-    _run(fn, args, what)
+    _run(*_cache_args(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_neox, mrope_section, stream,
+                      cache_mode, query_out, key_out))
 
 
 def _cache_args(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_neox, mrope_section, stream,
@@ -209,9 +241,10 @@ def _cache_args(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_
     cache_mode 0, else V2."""
     lib = load()
     R = int(cos_sin_cache.shape[1]) if rotary_dim is None else int(rotary_dim)
-    dp, dc = tensor_desc(positions), tensor_desc(cos_sin_cache)
+    _one_device(query, key, positions, cos_sin_cache, query_out, key_out)
     dq, qs = rows_desc(query)
     dk, ks = rows_desc(key)
+    dp, dc = tensor_desc(positions), tensor_desc(cos_sin_cache)
     sec = None
     n_sec = 0
     if mrope_section is not None:
@@ -236,8 +269,10 @@ def _cache_args(positions, query, key, cos_sin_cache, head_size, rotary_dim, is_
 
 def _qkv_args(qkv, num_q_heads, num_k_heads, num_v_heads, q_gamma, k_gamma, eps, cos_sin_cache, seq_lens,
               query_start_loc, slot_mapping, q_out, k_cache, v_cache, stream):
-    descs = [tensor_desc(t) for t in (qkv, q_gamma, k_gamma, cos_sin_cache, seq_lens, query_start_loc,
-                                      slot_mapping, q_out, k_cache, v_cache)]
+    tensors = (qkv, q_gamma, k_gamma, cos_sin_cache, seq_lens, query_start_loc, slot_mapping, q_out, k_cache,
+               v_cache)
+    _one_device(*tensors)
+    descs = [tensor_desc(t) for t in tensors]
     r = [ctypes.byref(d) for d in descs]
     args = (r[0], int(num_q_heads), int(num_k_heads), int(num_v_heads), r[1], r[2], float(eps), r[3], r[4], r[5],
             r[6], r[7], r[8], r[9], _stream_handle(qkv, stream))
@@ -252,7 +287,7 @@ def qkv_rmsnorm_rope_cache(qkv: torch.Tensor, num_q_heads: int, num_k_heads: int
     lib = load()
     args, _ = _qkv_args(qkv, num_q_heads, num_k_heads, num_v_heads, q_gamma, k_gamma, eps, cos_sin_cache,
                         seq_lens, query_start_loc, slot_mapping, q_out, k_cache, v_cache, stream)
-    _run(lib.rope_qkv_rmsnorm_rope_cache, args, "rope_qkv_rmsnorm_rope_cache")
+    _run(lib.rope_qkv_rmsnorm_rope_cache, args, (qkv,), "rope_qkv_rmsnorm_rope_cache")
 
 
 def prepare_qkv_rmsnorm_rope_cache(qkv: torch.Tensor, num_q_heads: int, num_k_heads: int, num_v_heads: int,
@@ -270,13 +305,20 @@ def prepare_qkv_rmsnorm_rope_cache(qkv: torch.Tensor, num_q_heads: int, num_k_he
 
 
 def get_device_error(stream=None, device=None) -> int:
-    """Synchronise ``stream`` and read-and-clear the device error word."""
+    """Synchronise ``stream`` and read-and-clear the error word of its device
+    (``device``, else the stream's device, else the current device)."""
     lib = load()
-    if stream is None:
-        stream = torch.cuda.current_stream(device)
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    code = ctypes.c_int32(0)
-    st = lib.rope_get_device_error(handle, ctypes.byref(code))
+    if device is None and stream is not None and hasattr(stream, "device"):
+        device = stream.device
+    dev = device if isinstance(device, int) else torch.device(device).index if device is not None else None
+    if dev is None:
+        dev = torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        if stream is None:
+            stream = torch.cuda.current_stream(dev)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        code = ctypes.c_int32(0)
+        st = lib.rope_get_device_error(handle, ctypes.byref(code))
     if st != ROPE_OK:
         raise RopeError(st, "rope_get_device_error")
     return int(code.value)
@@ -299,9 +341,13 @@ class PreparedCall:
         self._args = args
         self._keep = keep
         self._what = what
+        first = keep[0]
+        while isinstance(first, (tuple, list)):
+            first = first[0]
+        self._device = first.get_device()
 
     def __call__(self) -> None:
-        st = self._fn(*self._args)
+        st = _on_device(self._device, self._fn, self._args)
         if st != ROPE_OK:
             raise RopeError(st, self._what)
 

@@ -68,17 +68,37 @@ using rope::kI64;
 
 bool is_float(int32_t dt) { return dt == kF32 || dt == kF16 || dt == kBF16; }
 
+// Largest element count accepted: the byte size of any tensor (8 bytes per
+// element at most) and every element offset the kernels form stay in int64.
+constexpr int64_t kMaxElements = INT64_MAX / 8;
+
+// Product of the dims of a tensor that passed shape_ok().
 int64_t numel(const rope_tensor_t* t) {
   int64_t n = 1;
   for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
   return n;
 }
 
+// 1 to 4 non-negative dims whose product (taken in order) stays within
+// kMaxElements; a shape whose product overflows is rejected, not wrapped.
 bool shape_ok(const rope_tensor_t* t) {
   if (t->ndim < 1 || t->ndim > 4) return false;
-  for (int i = 0; i < t->ndim; ++i)
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) {
     if (t->shape[i] < 0) return false;
+    if (__builtin_mul_overflow(n, t->shape[i], &n) || n > kMaxElements) return false;
+  }
   return true;
+}
+
+// Elements spanned by `rows` rows of `width` elements, `stride` apart:
+// (rows - 1) * stride + width, or -1 when that leaves kMaxElements.
+int64_t strided_extent(int64_t rows, int64_t stride, int64_t width) {
+  int64_t n = 0;
+  if (rows <= 0) return 0;
+  if (__builtin_mul_overflow(rows - 1, stride, &n) || __builtin_add_overflow(n, width, &n) || n > kMaxElements)
+    return -1;
+  return n;
 }
 
 bool aligned(const void* p, uintptr_t bytes) { return reinterpret_cast<uintptr_t>(p) % bytes == 0; }
@@ -182,7 +202,8 @@ int cache_call(const rope_tensor_t* positions, const rope_tensor_t* query, const
   const int64_t qw = query->shape[1], kw = key->shape[1];
   const int64_t qs = q_row_stride ? q_row_stride : qw, ks = k_row_stride ? k_row_stride : kw;
   const int64_t esz = query->dtype == kF32 ? 4 : 2;
-  if (qs < qw || ks < kw || (qs * esz) % 16 || (ks * esz) % 16) return ROPE_ERR_PARAM_INVALID;
+  if (qs < qw || ks < kw || qs % (16 / esz) || ks % (16 / esz)) return ROPE_ERR_PARAM_INVALID;
+  if (strided_extent(T, qs, qw) < 0 || strided_extent(T, ks, kw) < 0) return ROPE_ERR_PARAM_INVALID;
   // outputs: both or neither; contiguous, same shape and dtype as the inputs
   if ((query_out == nullptr) != (key_out == nullptr)) return ROPE_ERR_PARAM_NULLPTR;
   if (query_out) {
@@ -275,6 +296,8 @@ int qkv_call(const rope_tensor_t* qkv, int64_t nq, int64_t nk, int64_t nv, const
   if (NB < 1 || BS < 1 || k_cache->shape[1] != nk || k_cache->shape[3] != D || v_cache->shape[0] != NB ||
       v_cache->shape[1] != nv || v_cache->shape[2] != BS || v_cache->shape[3] != D)
     return ROPE_ERR_PARAM_INVALID;
+  int64_t slots = 0;  // NB * BS, also when a cache has no heads (and so no elements)
+  if (__builtin_mul_overflow(NB, BS, &slots) || slots > kMaxElements) return ROPE_ERR_PARAM_INVALID;
   // head counts and the block size are kept in 32-bit fields by the kernel
   if (nq + nk + nv > (int64_t(1) << 30) || BS > (int64_t(1) << 30)) return ROPE_ERR_PARAM_INVALID;
   if (!(eps >= 0.0f) || !(eps < 1e30f)) return ROPE_ERR_PARAM_INVALID;

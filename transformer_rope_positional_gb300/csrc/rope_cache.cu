@@ -34,6 +34,12 @@ namespace rope {
 // Device-side error word (one per device context), read and cleared by
 // read_and_clear_device_error().
 __device__ unsigned int g_device_error;
+// The value the last read-and-clear took from g_device_error.
+__device__ unsigned int g_device_error_taken;
+
+// Atomically takes the error word and leaves zero in it, so that a bit set by
+// a kernel on another stream is either taken now or kept for the next read.
+__global__ void take_device_error_kernel() { g_device_error_taken = atomicExch(&g_device_error, 0u); }
 
 namespace {
 
@@ -369,12 +375,15 @@ cudaError_t device_error_address(unsigned int** out) {
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t* code) {
+  // one reader at a time: the taken value sits in one device word until copied out
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
   unsigned int host = 0;
-  const unsigned int zero = 0;
-  cudaError_t e = cudaMemcpyFromSymbolAsync(&host, g_device_error, sizeof(host), 0,
-                                            cudaMemcpyDeviceToHost, stream);
+  take_device_error_kernel<<<1, 1, 0, stream>>>();
+  count_launch();
+  cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
-    e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+    e = cudaMemcpyFromSymbolAsync(&host, g_device_error_taken, sizeof(host), 0, cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   *code = host;
   return e;
