@@ -307,6 +307,7 @@ def run_ours(args):
     del specs
     for entry in next_rows:
         entry.update(streams.get(entry["workload"], {}))
+    small = time_small_rows(dev)
     sampler.stop()
     clocks = sampler.summary(t_host0, t_host1)
     ms_step_local = total_ms / K
@@ -358,13 +359,111 @@ def run_ours(args):
                            "l2": "inputs larger than L2: %.2f GB per step vs %d MB L2; each kernel's buffers are "
                                  "evicted by the others between its launches" % (total_bytes / 1e9, L2_BYTES >> 20),
                            "parallelism": "replicas of the per-GPU workload (weak scaling), no collective"},
-                "per_kernel": kernels, "next_rows": next_rows, "roofline": roofline, "e2e": e2e,
+                "per_kernel": kernels, "next_rows": next_rows, "small_rows": small, "roofline": roofline, "e2e": e2e,
                 "gpu_launches": launches,
                 "clocks": clocks, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+DECODE_TOKENS = (1, 8, 64, 256)
+GRAPH_LAUNCHES = 100
+
+
+def small_workloads():
+    """Latency-bound calls: the small in-place workload (slice [16,48), the
+    whole-D [0,0] variant and the [8,8] no-op) and decode-sized batches of the
+    cache operator on the head layouts of the three cache workloads."""
+    import workloads as W
+    out = [W.inplace_f32_small(v) for v in ("slice", "full", "noop")]
+    for T in DECODE_TOKENS:
+        out.append(W.cache_case("decode_rope_neox_bf16_%dtok_32q8k_h128" % T, 20, T, 32, 8, 128, 128, 32768,
+                                torch.bfloat16, True))
+        out.append(W.cache_case("decode_rope_gptj_f16_%dtok_16q16k_h256_r64" % T, 21, T, 16, 16, 256, 64, 65536,
+                                torch.float16, False))
+        out.append(W.cache_case("decode_mrope_neox_bf16_%dtok_28q4k_h128_s16_24_24" % T, 22, T, 28, 4, 128, 128,
+                                40960, torch.bfloat16, True, base=1e6, mrope_section=[16, 24, 24]))
+    return out
+
+
+def latency_us(enqueue, reps: int = 200):
+    """(median evented us, us per launch replayed from a CUDA graph) of a call
+    that ``enqueue()`` puts on the current stream.  Evented: each call between
+    two events, all queued behind a sleep kernel so that the host's own time
+    per call never shows.  Graph: GRAPH_LAUNCHES calls captured once, the graph
+    replayed 20 times between two events (the device's time per call, launch
+    overhead included, with no host in the loop)."""
+    for _ in range(5):
+        enqueue()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda._sleep(int(7e4 * reps))  # about 35 us of queueing time per call
+    for e0, e1 in ev:
+        e0.record()
+        enqueue()
+        e1.record()
+    torch.cuda.synchronize()
+    evented = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(GRAPH_LAUNCHES):
+                enqueue()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record()
+    for _ in range(20):
+        graph.replay()
+    g1.record()
+    torch.cuda.synchronize()
+    return evented, g0.elapsed_time(g1) / (20 * GRAPH_LAUNCHES) * 1e3
+
+
+def time_small_rows(dev):
+    """Per-call latency of the small workloads, next to the floor of an empty
+    kernel launch timed the same two ways."""
+    import transformer_rope_positional_gb300 as R
+    floor_ev, floor_graph = latency_us(lambda: torch.cuda._sleep(0))
+    rows = []
+    for c in small_workloads():
+        if hasattr(c, "x"):
+            t = (c.x.to(dev), c.cos.to(dev), c.sin.to(dev))
+            enqueue = (lambda t=t, c=c: R.rope_inplace_partial(t[0], t[1], t[2], c.rotary_mode, [c.start, c.end]))
+        else:
+            t = (c.positions.to(dev), c.query.to(dev), c.key.to(dev), c.cache.to(dev))
+            enqueue = (lambda t=t, c=c: R.rope_with_sin_cos_cache(t[0], t[1], t[2], t[3], c.head_size, c.rotary_dim,
+                                                                 c.is_neox, c.mrope_section))
+        torch.cuda.synchronize()
+        l0 = R.launch_count()
+        enqueue()
+        torch.cuda.synchronize()
+        launches = R.launch_count() - l0
+        row = {"workload": c.name, "tokens": c.tokens, "launches_per_call": launches}
+        if launches == 0:  # the no-op: the call returns before any CUDA call
+            h0 = time.perf_counter()
+            for _ in range(1000):
+                enqueue()
+            row.update({"bytes_per_call": 0, "host_us_per_call": round((time.perf_counter() - h0) * 1e3, 3)})
+            rows.append(row)
+            continue
+        nbytes = algorithmic_bytes(c)
+        ev, gr = latency_us(enqueue)
+        row.update({"bytes_per_call": nbytes, "evented_us": round(ev, 3), "graph_us": round(gr, 3),
+                    "tokens_per_s": round(c.tokens / (gr * 1e-6), 1), "gbs": round(nbytes / (gr * 1e-6) / 1e9, 2),
+                    "floor_over_evented": round(floor_ev / ev, 3), "floor_over_graph": round(floor_graph / gr, 3)})
+        rows.append(row)
+        del t
+    return {"empty_kernel_floor": {"evented_us": round(floor_ev, 3), "graph_us": round(floor_graph, 3),
+                                   "kernel": "torch.cuda._sleep(0), a kernel that returns at once"},
+            "method": "evented: median of 200 calls each between two events, queued behind a sleep kernel; "
+                      "graph: %d calls replayed from one CUDA graph, per call" % GRAPH_LAUNCHES,
+            "rows": rows}
 
 
 def copies(*ts, n):
@@ -598,77 +697,285 @@ def oracle_sample(case, tokens: int):
 
 
 def run_oracle(case):
+    """The oracle on one workload; returns its outputs (x, or (query, key))."""
     import oracle
     if hasattr(case, "x"):
-        oracle.inplace_partial_rotary_mul(case.x, case.cos, case.sin, case.start, case.end)
-    else:
-        oracle.rope_with_sin_cos_cache(case.positions, case.query, case.key, case.cache, case.head_size,
-                                       case.is_neox, case.mrope_section)
+        return oracle.inplace_partial_rotary_mul(case.x, case.cos, case.sin, case.start, case.end)
+    return oracle.rope_with_sin_cos_cache(case.positions, case.query, case.key, case.cache, case.head_size,
+                                          case.is_neox, case.mrope_section)[:2]
 
 
-def time_oracle(samples):
-    t0 = time.perf_counter()
-    for s in samples:
-        run_oracle(s)
-    return time.perf_counter() - t0
+def _bounds(n: int, parts: int):
+    parts = max(1, min(parts, n))
+    return [(n * i // parts, n * (i + 1) // parts) for i in range(parts)]
 
 
-def sized_samples(cases, budget_s: float):
-    """Per-workload token samples whose oracle time adds up to about budget_s,
-    keeping each workload's share of the step's bytes."""
+def oracle_shards(case, parts: int):
+    """A workload cut into ``parts`` contiguous token ranges (in-place op:
+    ranges of S, with cos/sin cut alongside unless broadcast over S; cache op:
+    ranges of tokens), each a standalone workload.  Tokens are independent
+    under both operators, so the shards' outputs put together are the whole
+    workload's."""
+    import workloads as W
+    if hasattr(case, "x"):
+        S = case.x.shape[1]
+        out = []
+        for s0, s1 in _bounds(S, parts):
+            cut = (lambda t: t[:, s0:s1].contiguous()) if case.cos.shape[1] != 1 else (lambda t: t)
+            out.append(W.InplaceCase(case.name, case.x[:, s0:s1].contiguous(), cut(case.cos), cut(case.sin),
+                                     case.start, case.end))
+        return out
+    return [W.CacheCase(case.name, case.positions[..., t0:t1].contiguous(), case.query[t0:t1].contiguous(),
+                        case.key[t0:t1].contiguous(), case.cache, case.head_size, case.rotary_dim, case.is_neox,
+                        case.mrope_section) for t0, t1 in _bounds(case.tokens, parts)]
+
+
+def run_oracle_threaded(case, threads: int, pool=None):
+    """The oracle on ``threads`` token shards of ``case`` at once, outputs put
+    back together.  A thin driver: the oracle's arithmetic is unchanged, each
+    shard is one plain call, and the C code runs without the GIL."""
+    import concurrent.futures as cf
+    shards = oracle_shards(case, threads)
+    own = pool is None
+    pool = pool or cf.ThreadPoolExecutor(max_workers=threads)
+    try:
+        outs = list(pool.map(run_oracle, shards))
+    finally:
+        if own:
+            pool.shutdown()
+    if hasattr(case, "x"):
+        return torch.cat(outs, 1)
+    return torch.cat([o[0] for o in outs], 0), torch.cat([o[1] for o in outs], 0)
+
+
+def usable_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def host_cpu() -> dict:
+    """nproc, the cores this process may use, and the CPU model (lscpu, else
+    /proc/cpuinfo)."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu model")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count(), "usable_cores": usable_cores(), "cpu_model": model or "unknown",
+            "machine": platform.machine()}
+
+
+def time_oracle(samples, threads: int = 1):
+    """Seconds of oracle work over the samples: one thread in order, or every
+    sample's token shards spread over ``threads`` threads (shards cut before
+    the clock starts)."""
+    if threads <= 1:
+        t0 = time.perf_counter()
+        for s in samples:
+            run_oracle(s)
+        return time.perf_counter() - t0
+    import concurrent.futures as cf
+    shards = [sh for s in samples for sh in oracle_shards(s, 4 * threads)]
+    with cf.ThreadPoolExecutor(max_workers=threads) as pool:
+        t0 = time.perf_counter()
+        list(pool.map(run_oracle, shards))
+        return time.perf_counter() - t0
+
+
+def sized_samples(cases, budget_s: float, threads: int = 1):
+    """Per-workload token samples whose oracle time on ``threads`` threads adds
+    up to about budget_s, keeping each workload's share of the step's bytes."""
     probe = [oracle_sample(c, 64) for c in cases]
     t = time_oracle(probe)
     probe_bytes = sum(algorithmic_bytes(p) for p in probe)
-    rate = probe_bytes / max(t, 1e-6)
+    rate = probe_bytes / max(t, 1e-6) * threads
     total = sum(algorithmic_bytes(c) for c in cases)
     frac = min(1.0, budget_s * rate / total)
     return [oracle_sample(c, max(1, int(c.tokens * frac))) for c in cases], frac
 
 
-def cpu_baseline(cases, budget_s: float):
-    import oracle
-    oracle.build()
-    samples, frac = sized_samples(cases, budget_s)
-    secs = time_oracle(samples)
+def _sample_text(samples, cases, threads):
     b = sum(algorithmic_bytes(s) for s in samples)
     tok = sum(s.tokens for s in samples)
     total_tok = sum(c.tokens for c in cases)
-    return {"value": round(b / secs / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "tokens_per_s": round(tok / secs, 1), "seconds": round(secs, 2),
-            "sample": "leading tokens of each of the four workloads, %d of the step's %d tokens (%.1f%%), %d bytes; "
-                      "binary64 scalar C oracle, one thread" % (tok, total_tok, 100 * tok / total_tok, b)}
+    how = "one thread" if threads == 1 else "%d threads over token shards" % threads
+    return ("leading tokens of each of the four workloads, %d of the step's %d tokens (%.1f%%), %d bytes; "
+            "binary64 scalar C oracle, %s" % (tok, total_tok, 100 * tok / total_tok, b, how))
+
+
+def cpu_baseline(cases, budget_s: float):
+    """The oracle on the host cores: on every usable core (token shards, one
+    thread per core; the headline figure) and on one core."""
+    import oracle
+    oracle.build()
+    host = host_cpu()
+    threads = host["usable_cores"]
+    single, _ = sized_samples(cases, budget_s)
+    secs1 = time_oracle(single)
+    b1 = sum(algorithmic_bytes(s) for s in single)
+    many, _ = sized_samples(cases, budget_s, threads)
+    secs, reps = 0.0, 0
+    while reps < 1 or (secs < 2.0 and reps < 20):  # repeat a short sample for a stable figure
+        secs += time_oracle(many, threads)
+        reps += 1
+    b = sum(algorithmic_bytes(s) for s in many) * reps
+    tok = sum(s.tokens for s in many) * reps
+    return {"value": round(b / secs / 1e9, 5), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "tokens_per_s": round(tok / secs, 1), "seconds": round(secs, 2), "repeats": reps,
+            "nproc": host["nproc"], "cpu_model": host["cpu_model"], "machine": host["machine"],
+            "sample": _sample_text(many, cases, threads) + (", run %d times" % reps if reps > 1 else ""),
+            "single_core": {"value": round(b1 / secs1 / 1e9, 5), "unit": "GB/s", "cores": 1,
+                            "tokens_per_s": round(sum(s.tokens for s in single) / secs1, 1),
+                            "seconds": round(secs1, 2), "sample": _sample_text(single, cases, 1)}}
 
 
 def run_reference(args):
+    """The reference arm: the oracle, as it stands, on every usable host core
+    (token shards, one thread per core), bounded samples of the workload."""
     world, rank, local = dist_env()
     if rank != 0:
         return
     import oracle
     oracle.build()
+    host = host_cpu()
+    threads = host["usable_cores"]
     cases = build_workloads()
     steps = args.steps + args.warmup
     per_step = max(0.02, min(0.5, args.reference_seconds / max(1, steps)))
-    samples, frac = sized_samples(cases, per_step)
+    samples, frac = sized_samples(cases, per_step, threads)
     for _ in range(args.warmup):
-        time_oracle(samples)
-    times = [time_oracle(samples) for _ in range(args.steps)]
+        time_oracle(samples, threads)
+    times = [time_oracle(samples, threads) for _ in range(args.steps)]
     secs = sum(times) / len(times)
     b = sum(algorithmic_bytes(s) for s in samples)
     tok = sum(s.tokens for s in samples)
     value = b / secs / 1e9
-    total_tok = sum(c.tokens for c in cases)
-    sample = ("leading tokens of each of the four workloads per step, %d of the step's %d tokens (%.3f%%), "
-              "%d bytes; binary64 scalar C oracle, one thread" % (tok, total_tok, 100 * tok / total_tok, b))
+    sample = _sample_text(samples, cases, threads) + ", per step"
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "tokens_per_s": round(tok / secs, 1),
             "config": {"workload": WORKLOAD_NAME, "sample": sample},
-            "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "nproc": host["nproc"], "cpu_model": host["cpu_model"], "sample": sample},
             "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
+
+
+def run_stream_only(args):
+    """One operator of the bench alone: its launches back to back over the
+    rotating buffer copies of the stream region (at least 3x L2 of other data
+    between two uses of a copy), ``--warmup`` then ``--steps`` launches, for a
+    profiler capture of consecutive launches in steady state (each launch's
+    DRAM write-back of the previous one's dirty lines included)."""
+    import math
+    from transformer_rope_positional_gb300 import build as B
+    B.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cases = build_workloads()
+    dev_tensors = []
+    for c in cases:
+        if hasattr(c, "x"):
+            dev_tensors.append((c.x.to(dev), c.cos.to(dev), c.sin.to(dev)))
+        else:
+            dev_tensors.append((c.positions.to(dev), c.query.to(dev), c.key.to(dev), c.cache.to(dev)))
+    specs = {label: (nbytes, factory) for label, nbytes, factory, _ in operator_specs(cases, dev_tensors)}
+    if args.stream_only not in specs:
+        raise SystemExit("unknown operator %r; one of %s" % (args.stream_only, ", ".join(sorted(specs))))
+    nbytes, factory = specs[args.stream_only]
+    n = max(2, math.ceil(3 * L2_BYTES / nbytes) + 1)
+    calls = factory(n)
+    for j in range(args.warmup):
+        calls[j % n]()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    host = []
+    e0.record()
+    for j in range(args.steps):
+        h0 = time.perf_counter()
+        calls[(args.warmup + j) % n]()
+        host.append((time.perf_counter() - h0) * 1e6)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / args.steps * 1e3
+    print(json.dumps({"mode": "stream_only", "workload": args.stream_only, "buffer_sets": n, "warmup": args.warmup,
+                      "launches": args.steps, "us_per_launch": round(us, 3), "bytes_per_launch": nbytes,
+                      "host_us_per_call": [round(h, 1) for h in host]}), flush=True)
+
+
+def run_fetch_granularity(args):
+    """The in-place workload's aligned slice [64,128) and the slice [4,68)
+    (which crosses a 128-byte line of every 256-byte row) under L2 fetch
+    granularity limits of 32, 64 and 128 bytes, set on this process's CUDA
+    context (cuCtxSetLimit; the setting ends with the process, and the
+    context's own value is restored at the end).  Default: stream time per
+    launch of each.  ``--steps 1``: one launch of each, for a profiler capture
+    of the DRAM bytes."""
+    import ctypes
+    import workloads as W
+    from transformer_rope_positional_gb300 import build as B
+    B.build()
+    import transformer_rope_positional_gb300 as R
+    limit_id = 0x05  # CU_LIMIT_MAX_L2_FETCH_GRANULARITY
+    cu = ctypes.CDLL("libcuda.so.1")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    torch.zeros(1, device=dev)  # the primary context is current on this thread
+
+    def limit():
+        v = ctypes.c_size_t(0)
+        if cu.cuCtxGetLimit(ctypes.byref(v), limit_id) != 0:
+            raise RuntimeError("cuCtxGetLimit failed")
+        return int(v.value)
+
+    def set_limit(n):
+        if cu.cuCtxSetLimit(limit_id, ctypes.c_size_t(n)) != 0:
+            raise RuntimeError("cuCtxSetLimit failed")
+
+    default = limit()
+    full = W.inplace_bf16_mixed()
+    cases = [full, W.inplace_case("inplace_bf16x_f32cs_4x4096x32x128_slice4_68", 1, tuple(full.x.shape), 4, 68,
+                                  torch.bfloat16, torch.float32)]
+    peak, _ = measured_peak()
+    rows = []
+    try:
+        for lim in (32, 64, 128):
+            set_limit(lim)
+            for c in cases:
+                x, cs, sn = c.x.to(dev), c.cos.to(dev), c.sin.to(dev)
+                row = {"workload": c.name, "fetch_limit_bytes": limit()}
+                if args.steps == 1:
+                    R.rope_inplace_partial(x, cs, sn, 1, [c.start, c.end])
+                    torch.cuda.synchronize()
+                else:
+                    nbytes = algorithmic_bytes(c)
+                    us = min(stream_us(lambda n: [R.prepare_inplace_partial(t[0], cs, sn, 1, [c.start, c.end])
+                                                  for t in copies(x, n=n)], nbytes)[0] for _ in range(3))
+                    row.update({"stream_us": round(us, 3), "frac_of_peak": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)})
+                rows.append(row)
+                del x
+                torch.cuda.empty_cache()
+    finally:
+        set_limit(default)
+    print(json.dumps({"mode": "fetch_granularity", "context_default_limit_bytes": default, "rows": rows}),
+          flush=True)
 
 
 def run_size_sweep(args):
@@ -829,11 +1136,19 @@ def main():
                     help="instead of the step: each kernel alone at 1x and 2x tokens on a clean L2")
     ap.add_argument("--size-sweep", action="store_true",
                     help="instead of the step: each operator stream-timed at 0.5x..2x tokens; rate and fixed cost")
+    ap.add_argument("--fetch-granularity", action="store_true",
+                    help="instead of the step: aligned and unaligned in-place slices under L2 fetch limits")
+    ap.add_argument("--stream-only", metavar="WORKLOAD",
+                    help="instead of the step: one operator's launches back to back (--warmup, then --steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.stream_only:
+        run_stream_only(args)
+    elif args.fetch_granularity:
+        run_fetch_granularity(args)
     elif args.marginal:
         run_marginal(args)
     elif args.size_sweep:

@@ -71,3 +71,27 @@ def test_committed_traffic_table_matches_the_sources():
     if not os.path.exists(path):
         pytest.skip("no traffic table")
     assert bench.recorded_traffic("mrope_neox_bf16_32768tok_28q4k_h128_s16_24_24") is not None
+
+
+def test_threaded_oracle_driver_is_bit_exact_with_one_thread():
+    """The all-cores CPU baseline cuts a workload into token shards and runs the
+    oracle on each in its own thread; the pieces put together are bit-exact with
+    one call on the whole workload."""
+    from parity import same_bits
+    inplace = W.inplace_case("shards_inplace", 31, (2, 37, 3, 64), 16, 48, torch.bfloat16, torch.float32)
+    per_head = W.inplace_case("shards_per_head", 32, (2, 9, 3, 32), 0, 0, torch.float16, torch.float16,
+                              cs_shape=(2, 9, 3, 32))
+    assert same_bits(bench.run_oracle_threaded(inplace, 5), bench.run_oracle(inplace))
+    assert same_bits(bench.run_oracle_threaded(per_head, 4), bench.run_oracle(per_head))
+    for c in (W.cache_case("shards_neox", 33, 101, 4, 2, 128, 64, 300, torch.bfloat16, True),
+              W.cache_case("shards_mrope", 34, 57, 3, 1, 128, 128, 200, torch.float32, True,
+                           mrope_section=[16, 24, 24])):
+        q1, k1 = bench.run_oracle(c)
+        qn, kn = bench.run_oracle_threaded(c, 6)
+        assert same_bits(qn, q1) and same_bits(kn, k1)
+    assert len(bench.oracle_shards(inplace, 100)) == 37  # never an empty shard
+
+
+def test_host_cpu_description():
+    h = bench.host_cpu()
+    assert h["nproc"] >= 1 and 1 <= h["usable_cores"] <= h["nproc"] and h["cpu_model"]
