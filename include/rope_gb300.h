@@ -78,7 +78,9 @@ enum {
 enum {
   ROPE_DEVICE_OK = 0,
   ROPE_DEVICE_POSITION_OUT_OF_RANGE = 1, /* some position was < 0 or >= maxSeqLen */
-  ROPE_DEVICE_SLOT_OUT_OF_RANGE = 2      /* some KV-cache slot was >= blocks * block size */
+  ROPE_DEVICE_SLOT_OUT_OF_RANGE = 2,     /* some KV-cache slot was >= blocks * block size */
+  ROPE_DEVICE_INDEX_OUT_OF_BOUNDS = 4    /* bounds-checking builds only: a kernel formed an address
+                                            outside the tensor it addresses (the access was skipped) */
 };
 
 /*

@@ -109,8 +109,9 @@ def compare_terms(got: torch.Tensor, ref: torch.Tensor, terms: np.ndarray, rel: 
     2^-24 of that sum, whatever cancellation happens in o.  Bound:
       float32:          |got - ref| <= rel * terms
       float16/bfloat16: |got - ref| <= 1 ulp(ref) + rel * terms
-    NaN matches NaN.  Returns the largest |got - ref| / terms, the largest ulp
-    distance, the element count and ``ok``."""
+    NaN matches NaN.  Returns the largest |got - ref| / bound (at most 1 when
+    ``ok``), the largest |got - ref| / terms, the largest ulp distance, the
+    element count and ``ok``."""
     g = got.detach().cpu().double().numpy()
     r = ref.detach().cpu().double().numpy()
     t = np.broadcast_to(np.asarray(terms, dtype=np.float64), r.shape)
@@ -123,8 +124,41 @@ def compare_terms(got: torch.Tensor, ref: torch.Tensor, terms: np.ndarray, rel: 
         bound = bound + ulp_of(ref)
     with np.errstate(divide="ignore", invalid="ignore"):
         scaled = np.where(err == 0, 0.0, err / t)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        of_bound = np.where(err == 0, 0.0, err / bound)
     ulps = ulp_distance(got, ref)
     return {"n": int(r.size), "ok": bool((err <= bound).all()),
+            "max_err_over_bound": float(of_bound.max()) if of_bound.size else 0.0,
             "max_err_over_terms": float(scaled.max()) if scaled.size else 0.0,
             "max_ulp": int(ulps.max()) if ulps.size else 0,
             "out_of_bound": int((err > bound).sum())}
+
+
+def assert_matches_rows(got: torch.Tensor, ref: torch.Tensor, what: str = "", rows: int = 1 << 16) -> None:
+    """assert_matches for large tensors: the same rules (float32: relative
+    error <= FP32_REL_TOL; half types: <= HALF_ULP_TOL ulps; NaN matches NaN,
+    +0 matches -0), evaluated with torch integer and float ops a block of rows
+    (last dim) at a time."""
+    assert got.shape == ref.shape and got.dtype == ref.dtype, (got.shape, ref.shape, got.dtype, ref.dtype)
+    g = got.detach().cpu().reshape(-1, got.shape[-1])
+    r = ref.detach().cpu().reshape(-1, ref.shape[-1])
+    for i in range(0, g.shape[0], rows):
+        gb, rb = g[i:i + rows], r[i:i + rows]
+        both_nan = torch.isnan(gb) & torch.isnan(rb)
+        one_nan = torch.isnan(gb) ^ torch.isnan(rb)
+        assert not bool(one_nan.any()), "%s rows %d..: NaN against a number" % (what, i)
+        if ref.dtype == torch.float32:
+            gd, rd = gb.double(), rb.double()
+            inf_ok = torch.isinf(rd) & (gd == rd)
+            rel = (gd - rd).abs() / rd.abs().clamp_min(2.0 ** -126)
+            rel = torch.where(both_nan | inf_ok, torch.zeros_like(rel), rel)
+            worst = float(torch.nan_to_num(rel, nan=float("inf")).max())
+            assert worst <= FP32_REL_TOL, "%s rows %d..: max relative error %g" % (what, i, worst)
+        else:
+            ia = gb.view(torch.int16).to(torch.int32)
+            ib = rb.view(torch.int16).to(torch.int32)
+            oa = torch.where(ia < 0, -(ia & 0x7FFF), ia)  # sign-magnitude -> ordered integers
+            ob = torch.where(ib < 0, -(ib & 0x7FFF), ib)
+            d = torch.where(both_nan, torch.zeros_like(oa), (oa - ob).abs())
+            worst = int(d.max())
+            assert worst <= HALF_ULP_TOL, "%s rows %d..: max %d ulp" % (what, i, worst)

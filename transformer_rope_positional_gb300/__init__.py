@@ -29,6 +29,7 @@ from ._capi import (  # noqa: F401
     qkv_rmsnorm_rope_cache,
     prepare_qkv_rmsnorm_rope_cache,
     ROPE_DEVICE_SLOT_OUT_OF_RANGE,
+    ROPE_DEVICE_INDEX_OUT_OF_BOUNDS,
     status_string,
 )
 

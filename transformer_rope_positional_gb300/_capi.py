@@ -14,7 +14,9 @@ from typing import Optional, Sequence
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "lib", "librope_gb300.so")
+# ROPE_GB300_DEBUG_BOUNDS=1 selects the bounds-checking debug build (see build.py)
+DEBUG_BOUNDS = os.environ.get("ROPE_GB300_DEBUG_BOUNDS", "0") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "lib", "librope_gb300_debug.so" if DEBUG_BOUNDS else "librope_gb300.so")
 
 F32, F16, BF16, I64 = 0, 1, 2, 3
 DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16, torch.int64: I64}
@@ -25,6 +27,7 @@ ROPE_ERR_PARAM_INVALID = 161002
 ROPE_ERR_CUDA = 561000
 ROPE_DEVICE_POSITION_OUT_OF_RANGE = 1
 ROPE_DEVICE_SLOT_OUT_OF_RANGE = 2
+ROPE_DEVICE_INDEX_OUT_OF_BOUNDS = 4
 
 EXPORTED = ("rope_inplace_partial", "rope_inplace_partial_backward", "rope_with_sin_cos_cache",
             "rope_with_sin_cos_cache_v2", "rope_qkv_rmsnorm_rope_cache", "rope_get_device_error",
@@ -52,8 +55,8 @@ def load() -> ctypes.CDLL:
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
-        raise RuntimeError("librope_gb300.so is not built (%s missing); run "
-                           "`python -m transformer_rope_positional_gb300.build`" % LIB_PATH)
+        raise RuntimeError("%s is not built; run `python -m transformer_rope_positional_gb300.build%s`"
+                           % (LIB_PATH, " --debug" if DEBUG_BOUNDS else ""))
     lib = ctypes.CDLL(LIB_PATH)
     P = ctypes.POINTER(RopeTensor)
     lib.rope_inplace_partial.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,

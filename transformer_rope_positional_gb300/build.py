@@ -1,9 +1,15 @@
 """Build ``librope_gb300.so`` in-tree with nvcc for sm_103a.
 
-Usage: ``python -m transformer_rope_positional_gb300.build [--force] [--verbose]``.
+Usage: ``python -m transformer_rope_positional_gb300.build [--force] [--verbose] [--debug]``.
 The translation units compile in parallel; the shared library lands in
 ``transformer_rope_positional_gb300/lib/``.  The CUDA runtime is linked
 statically, so the library needs only the driver at run time.
+
+``--debug`` builds ``librope_gb300_debug.so`` with ``-DROPE_DEBUG_BOUNDS``:
+every global access of every kernel is checked against the span of the tensor
+it addresses; an access outside it is skipped and recorded in the device error
+word (ROPE_DEVICE_INDEX_OUT_OF_BOUNDS).  The binding loads it instead of the
+release library when ``ROPE_GB300_DEBUG_BOUNDS=1`` is set.
 """
 from __future__ import annotations
 
@@ -21,6 +27,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "librope_gb300.so")
+DEBUG_LIB_PATH = os.path.join(LIB_DIR, "librope_gb300_debug.so")
 
 SOURCES = ["rope_api.cu", "rope_inplace_fwd.cu", "rope_inplace_bwd.cu", "rope_cache.cu", "rope_qkv.cu"]
 HEADERS = ["rope_device.cuh", "rope_launch.h", "rope_inplace.cuh"]
@@ -40,24 +47,27 @@ def _inputs():
     return srcs + [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "rope_gb300.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every translation unit and link the shared library."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile every translation unit and link the shared library (the
+    bounds-checking debug library with ``debug=True``)."""
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    if not force and up_to_date(lib_path):
+        return lib_path
+    build_dir = BUILD_DIR + ("_debug" if debug else "")
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if verbose else []
+    extra = (["-Xptxas", "-v"] if verbose else []) + (["-DROPE_DEBUG_BOUNDS"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -69,18 +79,19 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB_PATH + ".%d.tmp" % os.getpid()
+    tmp = lib_path + ".%d.tmp" % os.getpid()
     cmd = [cc, *ARCH, "-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true", help="print ptxas register/spill reports")
+    ap.add_argument("--debug", action="store_true", help="the bounds-checking debug library")
     args = ap.parse_args()
-    print(build(force=args.force, verbose=args.verbose))
+    print(build(force=args.force, verbose=args.verbose, debug=args.debug))

@@ -151,6 +151,7 @@ int inplace_call(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_te
   p.cs_n = cN == 1 ? 0 : 1;
   p.cs_s = cS == 1 ? 0 : cN;
   p.cs_b = cB == 1 ? 0 : cS * cN;
+  p.cs_rows = cB * cS * cN;
   return cuda_status(rope::launch_inplace(p, static_cast<cudaStream_t>(stream)));
 }
 

@@ -56,7 +56,17 @@ namespace {
 #ifndef ROPE_CACHE_MIN_BLOCKS_GPTJ
 #define ROPE_CACHE_MIN_BLOCKS_GPTJ 10
 #endif
-constexpr int kRowsInFlight = ROPE_CACHE_ROWS_IN_FLIGHT;  // U: rows loaded before compute, per thread
+#ifndef ROPE_CACHE_ROWS_GPTJ
+#define ROPE_CACHE_ROWS_GPTJ 4
+#endif
+#ifndef ROPE_CACHE_PREFETCH_GPTJ
+#define ROPE_CACHE_PREFETCH_GPTJ 0
+#endif
+// 0: the grid is every CTA that fits at once; 1: the fewest CTAs that still
+// take the same number of rounds of items (every row group gets an equal share)
+#ifndef ROPE_CACHE_EVEN_ROUNDS
+#define ROPE_CACHE_EVEN_ROUNDS 0
+#endif
 constexpr int kThreads = ROPE_CACHE_THREADS;
 constexpr unsigned kPositionOutOfRange = 1u;
 
@@ -75,6 +85,8 @@ struct CacheArgs {
   int32_t cache_mode;      // 0 sectioned splice, 1 interleaved splice (V2)
   int32_t interleave_end;  // cache_mode 1: indices below 3 * mropeSection[1] interleave
   bool items32;            // items fit 32-bit index arithmetic
+  // byte spans of the tensors (checked in debug builds)
+  Span pos_span, q_span, k_span, cache_span, qo_span, ko_span;
 };
 
 // Section holding cos index i.  section_end[] holds cumulative ends and the
@@ -92,13 +104,34 @@ __device__ __forceinline__ int64_t select_row(int k, int64_t p0, int64_t p1, int
 // spliced in order, mrope with the V2 interleaved splice.
 enum Splice : int { kRope = 0, kSectioned = 1, kInterleaved = 2 };
 
-// CTAs per SM asked of the compiler.  The in-place GPT-J rope kernel (one
-// vector per row and thread, a quarter of each row touched) is latency-bound:
-// 10 CTAs (48 registers, no spills) beat its uncapped 7; the other variants are
-// best uncapped (a cap spills them).
+// The in-place GPT-J rope kernel (one vector per row and thread, a quarter of
+// each row touched) is latency-bound and has its own settings.
+template <bool NEOX, bool OUT, int SPLICE>
+__host__ __device__ constexpr bool gptj_rope() {
+  return !NEOX && !OUT && SPLICE == kRope;
+}
+
+// CTAs per SM asked of the compiler: 10 for the GPT-J rope kernel (48
+// registers, no spills; beats its uncapped 7); the other variants are best
+// uncapped (a cap spills them).
 template <bool NEOX, bool OUT, int SPLICE>
 __host__ __device__ constexpr int min_blocks() {
-  return (!NEOX && !OUT && SPLICE == kRope) ? ROPE_CACHE_MIN_BLOCKS_GPTJ : ROPE_CACHE_MIN_BLOCKS;
+  return gptj_rope<NEOX, OUT, SPLICE>() ? ROPE_CACHE_MIN_BLOCKS_GPTJ : ROPE_CACHE_MIN_BLOCKS;
+}
+
+// U: head rows per item, all loaded before any arithmetic.
+template <bool NEOX, bool OUT, int SPLICE>
+__host__ __device__ constexpr int rows_per_item() {
+  return gptj_rope<NEOX, OUT, SPLICE>() ? ROPE_CACHE_ROWS_GPTJ : ROPE_CACHE_ROWS_IN_FLIGHT;
+}
+
+// Whether the next item's position rows are loaded while the current item is
+// processed (so the cos/sin gather leaves with the row loads): measured faster
+// for the in-place NeoX kernels; the out-of-place kernels lose an occupancy
+// step to the extra registers and are faster without it.
+template <bool NEOX, bool OUT, int SPLICE>
+__host__ __device__ constexpr bool prefetch_positions() {
+  return gptj_rope<NEOX, OUT, SPLICE>() ? ROPE_CACHE_PREFETCH_GPTJ != 0 : (NEOX && !OUT);
 }
 
 // The position rows of one token (rope: p[0] only; mrope: 3 or 4 rows).
@@ -109,13 +142,13 @@ struct TokenPos {
 template <int SPLICE>
 __device__ __forceinline__ TokenPos load_positions(const int64_t* __restrict__ pos, const CacheArgs& a, int64_t t) {
   TokenPos r;
-  r.p[0] = __ldg(pos + t);
+  r.p[0] = ldg(pos + t, a.pos_span, &g_device_error);
   if constexpr (SPLICE == kRope) {
     r.p[1] = r.p[2] = r.p[3] = 0;
   } else {
-    r.p[1] = __ldg(pos + a.T + t);
-    r.p[2] = __ldg(pos + 2 * a.T + t);
-    r.p[3] = a.mrope_rows > 3 ? __ldg(pos + 3 * a.T + t) : 0;
+    r.p[1] = ldg(pos + a.T + t, a.pos_span, &g_device_error);
+    r.p[2] = ldg(pos + 2 * a.T + t, a.pos_span, &g_device_error);
+    r.p[3] = a.mrope_rows > 3 ? ldg(pos + 3 * a.T + t, a.pos_span, &g_device_error) : 0;
   }
   return r;
 }
@@ -131,8 +164,8 @@ __device__ __forceinline__ bool gather_cos_sin(const TokenPos& tp, const T* __re
     const int64_t p = tp.p[0];
     if (p < 0 || p >= a.max_seq) return false;
     const T* rowp = cache + p * a.R;
-    load_f32<T, NC>(cf, rowp + i0);
-    load_f32<T, NC>(sf, rowp + half + i0);
+    load_f32<T, NC>(cf, rowp + i0, a.cache_span, &g_device_error);
+    load_f32<T, NC>(sf, rowp + half + i0, a.cache_span, &g_device_error);
     return true;
   }
   const int64_t p0 = tp.p[0], p1 = tp.p[1], p2 = tp.p[2], p3 = tp.p[3];
@@ -144,15 +177,15 @@ __device__ __forceinline__ bool gather_cos_sin(const TokenPos& tp, const T* __re
     // remainder mod 3 is 1 (row 1) or 2 (row 2)
     if (i0 >= a.interleave_end) {
       const T* rowp = cache + p0 * a.R;
-      load_f32<T, NC>(cf, rowp + i0);
-      load_f32<T, NC>(sf, rowp + half + i0);
+      load_f32<T, NC>(cf, rowp + i0, a.cache_span, &g_device_error);
+      load_f32<T, NC>(sf, rowp + half + i0, a.cache_span, &g_device_error);
     } else {
 #pragma unroll
       for (int e = 0; e < NC; ++e) {
         const int i = i0 + e;
         const T* rowp = cache + select_row(i < a.interleave_end ? i % 3 : 0, p0, p1, p2, p3) * a.R;
-        cf[e] = widen(__ldg(rowp + i));
-        sf[e] = widen(__ldg(rowp + half + i));
+        cf[e] = widen(ldg(rowp + i, a.cache_span, &g_device_error));
+        sf[e] = widen(ldg(rowp + half + i, a.cache_span, &g_device_error));
       }
     }
     return true;
@@ -161,14 +194,14 @@ __device__ __forceinline__ bool gather_cos_sin(const TokenPos& tp, const T* __re
   const int k1 = section_of(i0 + NC - 1, a);
   if (k0 == k1) {  // the whole chunk sits in one section: one vector per half
     const T* rowp = cache + select_row(k0, p0, p1, p2, p3) * a.R;
-    load_f32<T, NC>(cf, rowp + i0);
-    load_f32<T, NC>(sf, rowp + half + i0);
+    load_f32<T, NC>(cf, rowp + i0, a.cache_span, &g_device_error);
+    load_f32<T, NC>(sf, rowp + half + i0, a.cache_span, &g_device_error);
   } else {  // the chunk straddles a section boundary: per-element rows
 #pragma unroll
     for (int e = 0; e < NC; ++e) {
       const T* rowp = cache + select_row(section_of(i0 + e, a), p0, p1, p2, p3) * a.R;
-      cf[e] = widen(__ldg(rowp + i0 + e));
-      sf[e] = widen(__ldg(rowp + half + i0 + e));
+      cf[e] = widen(ldg(rowp + i0 + e, a.cache_span, &g_device_error));
+      sf[e] = widen(ldg(rowp + half + i0 + e, a.cache_span, &g_device_error));
     }
   }
   return true;
@@ -180,7 +213,7 @@ template <typename T, bool NEOX, bool OUT, int SPLICE, int VEC>
 __global__ void __launch_bounds__(kThreads, min_blocks<NEOX, OUT, SPLICE>())
     cache_kernel(const int64_t* __restrict__ pos, T* __restrict__ q, T* __restrict__ k,
                  const T* __restrict__ cache, T* __restrict__ qo, T* __restrict__ ko, CacheArgs a) {
-  constexpr int U = kRowsInFlight;
+  constexpr int U = rows_per_item<NEOX, OUT, SPLICE>();
   constexpr int NC = NEOX ? VEC : VEC / 2;  // cos (and sin) indices owned per thread
   const int C = a.chunks;
   const int P = blockDim.x / C;  // row groups per CTA
@@ -193,11 +226,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<NEOX, OUT, SPLICE>())
   wait_for_prior_grid();
 
   // item = (token t, head chunk j): heads [j*U, min(j*U + U, heads)) of token t.
-  // PREFETCH: the next item's position rows are loaded while this item is
-  // processed, so the cos/sin gather leaves with the row loads (measured faster
-  // for the in-place NeoX kernels; the GPT-J and out-of-place kernels lose an
-  // occupancy step to the extra registers and are faster without it).
-  constexpr bool PREFETCH = NEOX && !OUT;
+  constexpr bool PREFETCH = prefetch_positions<NEOX, OUT, SPLICE>();
   const int64_t stride = (int64_t)gridDim.x * P;
   int64_t item = (int64_t)blockIdx.x * P + g;
   int64_t t = 0;
@@ -214,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<NEOX, OUT, SPLICE>())
     const int n = min(U, heads - h0);
     // ---- issue the loads of the chunk's rows
     T* base[U];
+    auto row_span = [&](int u) -> const Span& { return h0 + u < a.hq ? a.q_span : a.k_span; };
     Vec<T, VEC> x1[U], x2[U];  // GPT-J uses x1 only
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -222,10 +252,10 @@ __global__ void __launch_bounds__(kThreads, min_blocks<NEOX, OUT, SPLICE>())
                          : k + t * a.k_stride + (h - a.hq) * (int64_t)a.head_size;
       if (u < n) {
         if constexpr (NEOX) {
-          load_vec<true>(x1[u], base[u] + i0);
-          load_vec<true>(x2[u], base[u] + half + i0);
+          load_vec<true>(x1[u], base[u] + i0, row_span(u), &g_device_error);
+          load_vec<true>(x2[u], base[u] + half + i0, row_span(u), &g_device_error);
         } else {
-          load_vec<true>(x1[u], base[u] + 2 * i0);
+          load_vec<true>(x1[u], base[u] + 2 * i0, row_span(u), &g_device_error);
         }
       }
     }
@@ -250,11 +280,14 @@ __global__ void __launch_bounds__(kThreads, min_blocks<NEOX, OUT, SPLICE>())
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (u >= n) break;
-      T* dst = base[u];
+      T* const src = base[u];
+      T* dst = src;
+      const Span* dspan = &row_span(u);
       if constexpr (OUT) {
         const int h = h0 + u;
         dst = h < a.hq ? qo + (tt * a.hq + h) * (int64_t)a.head_size
                        : ko + (tt * a.hk + (h - a.hq)) * (int64_t)a.head_size;
+        dspan = h < a.hq ? &a.qo_span : &a.ko_span;
       }
       if constexpr (NEOX) {
 #pragma unroll
@@ -264,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, min_blocks<NEOX, OUT, SPLICE>())
           x1[u].e[e] = narrow<T>(diff_of_products(a1, cf[e], a2, sf[e]));
           x2[u].e[e] = narrow<T>(diff_of_products(a2, cf[e], -a1, sf[e]));
         }
-        store_vec(dst + i0, x1[u]);
-        store_vec(dst + half + i0, x2[u]);
+        store_vec(dst + i0, x1[u], *dspan, &g_device_error);
+        store_vec(dst + half + i0, x2[u], *dspan, &g_device_error);
       } else {
 #pragma unroll
         for (int e = 0; e < NC; ++e) {
@@ -274,14 +307,14 @@ __global__ void __launch_bounds__(kThreads, min_blocks<NEOX, OUT, SPLICE>())
           x1[u].e[2 * e] = narrow<T>(diff_of_products(a1, cf[e], a2, sf[e]));
           x1[u].e[2 * e + 1] = narrow<T>(diff_of_products(a2, cf[e], -a1, sf[e]));
         }
-        store_vec(dst + 2 * i0, x1[u]);
+        store_vec(dst + 2 * i0, x1[u], *dspan, &g_device_error);
       }
       if constexpr (OUT) {
         // pass-through columns [R, head_size) are copied to the output row
         for (int j = a.R + c * VEC; j < a.head_size; j += C * VEC) {
           Vec<T, VEC> v;
-          load_vec<true>(v, base[u] + j);
-          store_vec(dst + j, v);
+          load_vec<true>(v, src + j, row_span(u), &g_device_error);
+          store_vec(dst + j, v, *dspan, &g_device_error);
         }
       }
     }
@@ -291,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<NEOX, OUT, SPLICE>())
 template <typename T, bool NEOX, bool OUT, int SPLICE>
 cudaError_t launch_typed(const CacheProblem& p, cudaStream_t stream) {
   constexpr int VEC = 16 / sizeof(T);
+  constexpr int U = rows_per_item<NEOX, OUT, SPLICE>();
   CacheArgs a;
   a.T = p.T;
   a.max_seq = p.max_seq;
@@ -306,16 +340,27 @@ cudaError_t launch_typed(const CacheProblem& p, cudaStream_t stream) {
   for (int i = 0; i < 4; ++i) a.section_end[i] = i < p.mrope_rows ? p.section_end[i] : (int32_t)(p.rotary_dim / 2);
   a.cache_mode = p.cache_mode;
   a.interleave_end = p.cache_mode == 1 ? 3 * (p.section_end[1] - p.section_end[0]) : 0;
-  a.head_chunks = (int32_t)((p.hq + p.hk + kRowsInFlight - 1) / kRowsInFlight);
+  a.head_chunks = (int32_t)((p.hq + p.hk + U - 1) / U);
   a.items = p.T * a.head_chunks;
   a.items32 = a.items <= 0xffffffffLL;
+  const int64_t e = sizeof(T), qw = p.hq * p.head_size, kw = p.hk * p.head_size;
+  a.pos_span = make_span(p.positions, (p.mrope_rows ? p.mrope_rows : 1) * p.T * 8);
+  a.q_span = make_span(p.query, ((p.T - 1) * p.q_stride + qw) * e);
+  a.k_span = make_span(p.key, ((p.T - 1) * p.k_stride + kw) * e);
+  a.cache_span = make_span(p.cache, p.max_seq * p.rotary_dim * e);
+  a.qo_span = make_span(p.query_out, p.T * qw * e);
+  a.ko_span = make_span(p.key_out, p.T * kw * e);
   const int threads = kThreads;
   const int64_t groups = threads / a.chunks;
   // Persistent grid: the CTAs that fit on the GPU at once stride over the items,
   // P consecutive items per CTA per step.
   auto kernel = cache_kernel<T, NEOX, OUT, SPLICE, VEC>;
   const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), threads);
-  const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
+  int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
+  if (ROPE_CACHE_EVEN_ROUNDS) {
+    const int64_t rounds = (a.items + grid * groups - 1) / (grid * groups);
+    grid = std::max<int64_t>(1, (a.items + rounds * groups - 1) / (rounds * groups));
+  }
   return launch_overlapped(kernel, (unsigned)grid, threads, stream, p.positions, static_cast<T*>(p.query),
                            static_cast<T*>(p.key), static_cast<const T*>(p.cache), static_cast<T*>(p.query_out),
                            static_cast<T*>(p.key_out), a);

@@ -52,6 +52,51 @@ __device__ __forceinline__ void narrow2(__nv_bfloat16* p, float2 v) {
   *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
 }
 
+// ---------------------------------------------------------------------------
+// Bounds checking (debug builds, -DROPE_DEBUG_BOUNDS).  Every global access of
+// the kernels goes through access_ok() with the byte span of the tensor it
+// addresses.  In a debug build an access that leaves its span is skipped (a
+// skipped load yields zeros) and sets kIndexOutOfBounds in the device error
+// word; nothing traps.  In a release build the spans are empty structs and
+// access_ok() is the constant true, so the check costs nothing.
+// ---------------------------------------------------------------------------
+constexpr unsigned kIndexOutOfBounds = 4u;
+
+struct Span {
+#ifdef ROPE_DEBUG_BOUNDS
+  const char* lo;
+  const char* hi;  // one past the last byte
+#endif
+};
+
+// The span [p, p + bytes) (host side).
+inline Span make_span(const void* p, int64_t bytes) {
+  Span s;
+#ifdef ROPE_DEBUG_BOUNDS
+  s.lo = static_cast<const char*>(p);
+  s.hi = static_cast<const char*>(p) + (bytes > 0 ? bytes : 0);
+#else
+  (void)p;
+  (void)bytes;
+#endif
+  return s;
+}
+
+__device__ __forceinline__ bool access_ok(const void* p, int bytes, const Span& s, unsigned int* err) {
+#ifdef ROPE_DEBUG_BOUNDS
+  const char* c = static_cast<const char*>(p);
+  if (c >= s.lo && c + bytes <= s.hi) return true;
+  atomicOr(err, kIndexOutOfBounds);
+  return false;
+#else
+  (void)p;
+  (void)bytes;
+  (void)s;
+  (void)err;
+  return true;
+#endif
+}
+
 // Quotient of a non-negative index by a positive divisor, in 32-bit
 // arithmetic when the host has checked that both fit (much cheaper than the
 // 64-bit division sequence).
@@ -142,6 +187,39 @@ __device__ __forceinline__ void load_f32(float (&out)[N], const T* p) {
   load_vec<false>(v, p);
 #pragma unroll
   for (int i = 0; i < N; ++i) out[i] = widen(v.e[i]);
+}
+
+// The same accesses with the bounds check of access_ok() (a no-op in release
+// builds; in debug builds a skipped load yields zeros).
+template <bool STREAM, typename T, int N>
+__device__ __forceinline__ void load_vec(Vec<T, N>& v, const T* p, const Span& s, unsigned int* err) {
+  if (access_ok(p, N * sizeof(T), s, err)) {
+    load_vec<STREAM>(v, p);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v.e[i] = T(0.0f);
+  }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void store_vec(T* p, const Vec<T, N>& v, const Span& s, unsigned int* err) {
+  if (access_ok(p, N * sizeof(T), s, err)) store_vec(p, v);
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void load_f32(float (&out)[N], const T* p, const Span& s, unsigned int* err) {
+  if (access_ok(p, N * sizeof(T), s, err)) {
+    load_f32<T, N>(out, p);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) out[i] = 0.0f;
+  }
+}
+
+// Scalar read-only load (zero when a debug build skips it).
+template <typename T>
+__device__ __forceinline__ T ldg(const T* p, const Span& s, unsigned int* err) {
+  return access_ok(p, sizeof(T), s, err) ? __ldg(p) : T(0);
 }
 
 }  // namespace rope

@@ -65,6 +65,8 @@ struct InplaceArgs {
   int32_t head_chunks;  // ceil(N / U): chunks of U consecutive heads per token
   int32_t chunks;       // threads per row
   bool items32;         // items (and so tokens) fit 32-bit index arithmetic
+  Span xs, coss, sins;  // byte spans of x, cos and sin (checked in debug builds)
+  unsigned int* err;    // device error word (debug builds; NULL otherwise)
 };
 
 // One pair (a at slot j, b at its partner j') with element-wise cos/sin.
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(512, ROPE_INPLACE_MIN_BLOCKS)
     for (int u = 0; u < U; ++u)
       if (u < n) {
 #pragma unroll
-        for (int v = 0; v < NV; ++v) load_vec<true>(xv[u][v], xrow + u * a.D + v * half);
+        for (int v = 0; v < NV; ++v) load_vec<true>(xv[u][v], xrow + u * a.D + v * half, a.xs, a.err);
       }
     if constexpr (PER_HEAD_CS) {
       Vec<TC, VEC> cv[U][NV], sv[U][NV];
@@ -146,8 +148,8 @@ __global__ void __launch_bounds__(512, ROPE_INPLACE_MIN_BLOCKS)
           const int64_t o = coff + (int64_t)(h0 + u) * a.cs_n * a.L;
 #pragma unroll
           for (int v = 0; v < NV; ++v) {
-            load_vec<false>(cv[u][v], cosp + o + v * half);
-            load_vec<false>(sv[u][v], sinp + o + v * half);
+            load_vec<false>(cv[u][v], cosp + o + v * half, a.coss, a.err);
+            load_vec<false>(sv[u][v], sinp + o + v * half, a.sins, a.err);
           }
         }
 #pragma unroll
@@ -163,22 +165,22 @@ __global__ void __launch_bounds__(512, ROPE_INPLACE_MIN_BLOCKS)
           }
         rotate_chunk<TX, VEC, NV, HALF, BWD>(xv[u], cf, sf);
 #pragma unroll
-        for (int v = 0; v < NV; ++v) store_vec(xrow + u * a.D + v * half, xv[u][v]);
+        for (int v = 0; v < NV; ++v) store_vec(xrow + u * a.D + v * half, xv[u][v], a.xs, a.err);
       }
     } else {
       // one cos/sin chunk serves the item's heads
       float cf[NV][VEC], sf[NV][VEC];
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
-        load_f32<TC, VEC>(cf[v], cosp + coff + v * half);
-        load_f32<TC, VEC>(sf[v], sinp + coff + v * half);
+        load_f32<TC, VEC>(cf[v], cosp + coff + v * half, a.coss, a.err);
+        load_f32<TC, VEC>(sf[v], sinp + coff + v * half, a.sins, a.err);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (u >= n) break;
         rotate_chunk<TX, VEC, NV, HALF, BWD>(xv[u], cf, sf);
 #pragma unroll
-        for (int v = 0; v < NV; ++v) store_vec(xrow + u * a.D + v * half, xv[u][v]);
+        for (int v = 0; v < NV; ++v) store_vec(xrow + u * a.D + v * half, xv[u][v], a.xs, a.err);
       }
     }
   }
@@ -205,11 +207,17 @@ __global__ void __launch_bounds__(256) inplace_pair_kernel(TX* __restrict__ x, c
     const int64_t j2 = HALF ? q + pairs : 2 * q + 1;  // partner
     const int64_t co = (b * a.cs_b + s * a.cs_s + n * a.cs_n) * a.L;
     TX* p = x + r * a.D + a.start;
-    float va = widen(p[j]), vb = widen(p[j2]);
-    rotate_pair<BWD>(va, vb, widen(cosp[co + j]), widen(sinp[co + j]), widen(cosp[co + j2]),
-                     widen(sinp[co + j2]));
-    p[j] = narrow<TX>(va);
-    p[j2] = narrow<TX>(vb);
+    const bool ok = access_ok(p + j, sizeof(TX), a.xs, a.err) && access_ok(p + j2, sizeof(TX), a.xs, a.err);
+    float va = ok ? widen(p[j]) : 0.0f, vb = ok ? widen(p[j2]) : 0.0f;
+    // cos/sin element e of this pair's row (zero where a debug build skips the load)
+    auto cs = [&](const TC* base, const Span& span, int64_t e) -> float {
+      return access_ok(base + co + e, sizeof(TC), span, a.err) ? widen(base[co + e]) : 0.0f;
+    };
+    rotate_pair<BWD>(va, vb, cs(cosp, a.coss, j), cs(sinp, a.sins, j), cs(cosp, a.coss, j2), cs(sinp, a.sins, j2));
+    if (ok) {
+      p[j] = narrow<TX>(va);
+      p[j2] = narrow<TX>(vb);
+    }
   }
 }
 
@@ -217,6 +225,14 @@ inline bool aligned(const void* p, int64_t bytes) { return (reinterpret_cast<uin
 
 inline InplaceArgs base_args(const InplaceProblem& p) {
   InplaceArgs a{};
+  const int64_t xe = p.x_dtype == kF32 ? 4 : 2, ce = p.cs_dtype == kF32 ? 4 : 2;
+  a.xs = make_span(p.x, p.B * p.S * p.N * p.D * xe);
+  a.coss = make_span(p.cos, p.cs_rows * p.L * ce);
+  a.sins = make_span(p.sin, p.cs_rows * p.L * ce);
+  a.err = nullptr;
+#ifdef ROPE_DEBUG_BOUNDS
+  if (device_error_address(&a.err) != cudaSuccess) a.err = nullptr;
+#endif
   a.S = p.S;
   a.N = p.N;
   a.D = p.D;

@@ -22,6 +22,7 @@ struct InplaceProblem {
   int64_t start, L;
   // cos/sin row strides (in rows of L elements) for b, s, n; 0 on broadcast dims
   int64_t cs_b, cs_s, cs_n;
+  int64_t cs_rows;  // rows of L elements in cos (and sin): cB * cS * cN
 };
 
 // Cache-indexed RoPE of query[T, hq*hs] and key[T, hk*hs].

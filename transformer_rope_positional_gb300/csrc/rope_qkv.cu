@@ -73,6 +73,8 @@ struct QkvArgs {
   float eps;
   float inv_d;
   bool items32;  // items and slots fit 32-bit index arithmetic
+  // byte spans of the tensors (checked in debug builds)
+  Span qkv_span, qg_span, kg_span, cache_span, sl_span, qsl_span, slot_span, qo_span, kc_span, vc_span, tab_span;
 };
 
 // Token metadata of one item.
@@ -86,13 +88,16 @@ struct ItemMeta {
 
 // Batch of token t: the largest b in [0, B) with queryStartLoc[b] <= t.  `lo`
 // is a batch with queryStartLoc[lo] <= t (the previous answer for a smaller
-// or equal token, or 0): the common case is one comparison.
-__device__ __forceinline__ int find_batch(const int64_t* __restrict__ qsl, int B, int64_t t, int lo) {
-  if (lo + 1 < B && qsl[lo + 1] <= t) {
+// or equal token, or 0): the common case is one comparison.  `qsl` is the
+// global tensor or its copy in shared memory, spanned by `span`.
+__device__ __forceinline__ int find_batch(const int64_t* __restrict__ qsl, int B, int64_t t, int lo, const Span& span,
+                                          unsigned int* err) {
+  auto at = [&](int i) -> int64_t { return access_ok(qsl + i, 8, span, err) ? qsl[i] : 0; };
+  if (lo + 1 < B && at(lo + 1) <= t) {
     int l = lo + 1, h = B - 1;
     while (l < h) {
       const int mid = (l + h + 1) >> 1;
-      if (qsl[mid] <= t) l = mid; else h = mid - 1;
+      if (at(mid) <= t) l = mid; else h = mid - 1;
     }
     lo = l;
   }
@@ -102,17 +107,19 @@ __device__ __forceinline__ int find_batch(const int64_t* __restrict__ qsl, int B
 template <bool SHARED>
 __device__ __forceinline__ ItemMeta item_meta(int64_t item, const QkvArgs& a, const int64_t* __restrict__ tab,
                                               const int64_t* __restrict__ qsl, const int64_t* __restrict__ seq_lens,
-                                              const int64_t* __restrict__ slot_mapping, int cursor) {
+                                              const int64_t* __restrict__ slot_mapping, int cursor,
+                                              unsigned int* err) {
   ItemMeta m;
   m.t = div_index(item, a.per_token, a.items32);
   m.r = (int32_t)(item - m.t * a.per_token);
-  m.slot = __ldg(slot_mapping + m.t);
+  m.slot = ldg(slot_mapping + m.t, a.slot_span, err);
   if (SHARED) {
-    m.b = find_batch(tab, (int)a.B, m.t, cursor);
-    m.position = m.t + tab[a.B + 1 + m.b];
+    m.b = find_batch(tab, (int)a.B, m.t, cursor, a.tab_span, err);
+    const int64_t* d = tab + a.B + 1 + m.b;
+    m.position = m.t + (access_ok(d, 8, a.tab_span, err) ? *d : 0);
   } else {
-    m.b = find_batch(qsl, (int)a.B, m.t, cursor);
-    m.position = __ldg(seq_lens + m.b) - __ldg(qsl + m.b + 1) + m.t;
+    m.b = find_batch(qsl, (int)a.B, m.t, cursor, a.qsl_span, err);
+    m.position = ldg(seq_lens + m.b, a.sl_span, err) - ldg(qsl + m.b + 1, a.qsl_span, err) + m.t;
   }
   return m;
 }
@@ -137,17 +144,21 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
 
   // [0, B]: queryStartLoc; [B + 1, 2B]: seqLens[b] - queryStartLoc[b + 1]
   extern __shared__ int64_t s_tab[];
+#ifdef ROPE_DEBUG_BOUNDS
+  a.tab_span.lo = reinterpret_cast<const char*>(s_tab);
+  a.tab_span.hi = reinterpret_cast<const char*>(s_tab + (SHARED ? 2 * a.B + 1 : 0));
+#endif
   if (SHARED) {
-    for (int64_t i = threadIdx.x; i <= a.B; i += blockDim.x) s_tab[i] = __ldg(qsl + i);
+    for (int64_t i = threadIdx.x; i <= a.B; i += blockDim.x) s_tab[i] = ldg(qsl + i, a.qsl_span, err);
     for (int64_t i = threadIdx.x; i < a.B; i += blockDim.x)
-      s_tab[a.B + 1 + i] = __ldg(seq_lens + i) - __ldg(qsl + i + 1);
+      s_tab[a.B + 1 + i] = ldg(seq_lens + i, a.sl_span, err) - ldg(qsl + i + 1, a.qsl_span, err);
     __syncthreads();
   }
 
   const int64_t stride = (int64_t)gridDim.x * P;
   int64_t item = (int64_t)blockIdx.x * P + g;
   if (item >= a.items) return;
-  ItemMeta m = item_meta<SHARED>(item, a, s_tab, qsl, seq_lens, slot_mapping, 0);
+  ItemMeta m = item_meta<SHARED>(item, a, s_tab, qsl, seq_lens, slot_mapping, 0, err);
   for (; item < a.items; item += stride) {
     // ---- this item's heads: kind 0 q, 1 k, 2 v; h0 within the kind
     int kind, h0, nh, hg;
@@ -171,16 +182,17 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (u < n) {
-          load_vec<true>(x1[u], src + u * a.D);
-          load_vec<true>(x2[u], src + u * a.D + half);
+          load_vec<true>(x1[u], src + u * a.D, a.qkv_span, err);
+          load_vec<true>(x2[u], src + u * a.D + half, a.qkv_span, err);
         }
       if (rotate) {
         const T* cs = cache + m.position * a.D + i0;
-        load_vec<false>(cv, cs);
-        load_vec<false>(sv, cs + half);
+        load_vec<false>(cv, cs, a.cache_span, err);
+        load_vec<false>(sv, cs + half, a.cache_span, err);
         const T* gamma = (kind == 0 ? q_gamma : k_gamma) + i0;
-        load_vec<false>(g1, gamma);
-        load_vec<false>(g2, gamma + half);
+        const Span& gs = kind == 0 ? a.qg_span : a.kg_span;
+        load_vec<false>(g1, gamma, gs, err);
+        load_vec<false>(g2, gamma + half, gs, err);
       }
     }
     if (c == 0 && m.r == 0) {  // reported once per token
@@ -190,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
     // destination of head h0 and the distance between consecutive heads
     T* dst = nullptr;
     int64_t dstride = a.D;
+    const Span* dspan = kind == 0 ? &a.qo_span : kind == 1 ? &a.kc_span : &a.vc_span;
     if (kind == 0) {
       dst = q_out + (m.t * a.nq + h0) * (int64_t)a.D;
     } else if (cache_it) {
@@ -201,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
     }
     // ---- next item's metadata while the loads are in flight
     const int64_t next = item + stride;
-    const ItemMeta mn = next < a.items ? item_meta<SHARED>(next, a, s_tab, qsl, seq_lens, slot_mapping, m.b) : m;
+    const ItemMeta mn =
+        next < a.items ? item_meta<SHARED>(next, a, s_tab, qsl, seq_lens, slot_mapping, m.b, err) : m;
 
     if (work && rotate) {
       // RMSNorm: squares of every row of the item (independent chains), then
@@ -252,16 +266,16 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
             narrow2(&x1[u].e[j], __fmul2_rn(lo, inv2));
             narrow2(&x2[u].e[j], __fmul2_rn(hi, inv2));
           }
-          store_vec(dst + u * dstride + i0, x1[u]);
-          store_vec(dst + u * dstride + half + i0, x2[u]);
+          store_vec(dst + u * dstride + i0, x1[u], *dspan, err);
+          store_vec(dst + u * dstride + half + i0, x2[u], *dspan, err);
         }
       }
     } else if (work && active) {  // V: stored as is
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (u < n) {
-          store_vec(dst + u * dstride + i0, x1[u]);
-          store_vec(dst + u * dstride + half + i0, x2[u]);
+          store_vec(dst + u * dstride + i0, x1[u], *dspan, err);
+          store_vec(dst + u * dstride + half + i0, x2[u], *dspan, err);
         }
     }
     m = mn;
@@ -312,6 +326,18 @@ cudaError_t launch_typed(const QkvProblem& p, cudaStream_t stream) {
   a.eps = p.eps;
   a.inv_d = 1.0f / (float)p.D;
   a.items32 = a.items <= 0xffffffffLL && a.num_slots <= 0xffffffffLL;
+  const int64_t e = sizeof(T);
+  a.qkv_span = make_span(p.qkv, p.T * a.W * e);
+  a.qg_span = make_span(p.q_gamma, p.D * e);
+  a.kg_span = make_span(p.k_gamma, p.D * e);
+  a.cache_span = make_span(p.cache, p.max_seq * p.D * e);
+  a.sl_span = make_span(p.seq_lens, p.B * 8);
+  a.qsl_span = make_span(p.query_start_loc, (p.B + 1) * 8);
+  a.slot_span = make_span(p.slot_mapping, p.T * 8);
+  a.qo_span = make_span(p.q_out, p.T * p.nq * p.D * e);
+  a.kc_span = make_span(p.k_cache, p.num_blocks * p.nk * p.block_size * p.D * e);
+  a.vc_span = make_span(p.v_cache, p.num_blocks * p.nv * p.block_size * p.D * e);
+  a.tab_span = make_span(nullptr, 0);  // set in the kernel: the shared batch tables
   if (2 * p.B + 1 <= kSharedTable) return launch_tables<T, true>(p, a, stream);
   return launch_tables<T, false>(p, a, stream);
 }
