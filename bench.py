@@ -192,13 +192,23 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def source_tokens(text: str) -> str:
+    """C/CUDA source with comments removed and whitespace runs collapsed (the
+    sources hold no string literal containing a comment marker)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
+    """sha256[:16] of the kernel sources' code (comments and layout excluded),
+    so that a profile stays tied to the code it measured."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transformer_rope_positional_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + source_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -374,8 +384,9 @@ GRAPH_LAUNCHES = 100
 
 def small_workloads():
     """Latency-bound calls: the small in-place workload (slice [16,48), the
-    whole-D [0,0] variant and the [8,8] no-op) and decode-sized batches of the
-    cache operator on the head layouts of the three cache workloads."""
+    whole-D [0,0] variant and the [8,8] no-op), decode-sized batches of the
+    cache operator on the head layouts of the three cache workloads, and the
+    fused QKV op on decode batches (one new token per sequence)."""
     import workloads as W
     out = [W.inplace_f32_small(v) for v in ("slice", "full", "noop")]
     for T in DECODE_TOKENS:
@@ -385,6 +396,10 @@ def small_workloads():
                                 torch.float16, False))
         out.append(W.cache_case("decode_mrope_neox_bf16_%dtok_28q4k_h128_s16_24_24" % T, 22, T, 28, 4, 128, 128,
                                 40960, torch.bfloat16, True, base=1e6, mrope_section=[16, 24, 24]))
+    for T in DECODE_TOKENS:  # the fused op on T decode requests, one new token each
+        ctx = W.uniform_int(W.stream_seed(23, 3), T, 16, 1024).tolist()
+        out.append(W.qkv_case("decode_qkv_rmsnorm_rope_bf16_%dseq_32q8k8v_h128" % T, 23, [1] * T, ctx, 32, 8, 8, 128,
+                              16, torch.bfloat16))
     return out
 
 
@@ -425,6 +440,21 @@ def latency_us(enqueue, reps: int = 200):
     return evented, g0.elapsed_time(g1) / (20 * GRAPH_LAUNCHES) * 1e3
 
 
+def host_us(call, n: int = 1000) -> float:
+    """Host microseconds per call of ``call`` (binding and C ABI: argument checks,
+    marshalling and the launch itself), n calls in a row, the GPU synchronised
+    after them."""
+    for _ in range(10):
+        call()
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    for _ in range(n):
+        call()
+    us = (time.perf_counter() - h0) / n * 1e6
+    torch.cuda.synchronize()
+    return round(us, 2)
+
+
 def time_small_rows(dev):
     """Per-call latency of the small workloads, next to the floor of an empty
     kernel launch timed the same two ways."""
@@ -432,24 +462,30 @@ def time_small_rows(dev):
     floor_ev, floor_graph = latency_us(lambda: torch.cuda._sleep(0))
     rows = []
     for c in small_workloads():
-        if hasattr(c, "x"):
+        if hasattr(c, "qkv"):
+            t = [v.to(dev) for v in (c.qkv, c.q_gamma, c.k_gamma, c.cache, c.seq_lens, c.query_start_loc,
+                                     c.slot_mapping, c.q_out, c.k_cache, c.v_cache)]
+            enqueue = (lambda t=t, c=c: R.qkv_rmsnorm_rope_cache(t[0], c.nq, c.nk, c.nv, t[1], t[2], c.eps, *t[3:]))
+            prepared = R.prepare_qkv_rmsnorm_rope_cache(t[0], c.nq, c.nk, c.nv, t[1], t[2], c.eps, *t[3:])
+        elif hasattr(c, "x"):
             t = (c.x.to(dev), c.cos.to(dev), c.sin.to(dev))
             enqueue = (lambda t=t, c=c: R.rope_inplace_partial(t[0], t[1], t[2], c.rotary_mode, [c.start, c.end]))
+            prepared = R.prepare_inplace_partial(t[0], t[1], t[2], c.rotary_mode, [c.start, c.end])
         else:
             t = (c.positions.to(dev), c.query.to(dev), c.key.to(dev), c.cache.to(dev))
             enqueue = (lambda t=t, c=c: R.rope_with_sin_cos_cache(t[0], t[1], t[2], t[3], c.head_size, c.rotary_dim,
                                                                  c.is_neox, c.mrope_section))
+            prepared = R.prepare_with_sin_cos_cache(t[0], t[1], t[2], t[3], c.head_size, c.rotary_dim, c.is_neox,
+                                                    c.mrope_section)
         torch.cuda.synchronize()
         l0 = R.launch_count()
         enqueue()
         torch.cuda.synchronize()
         launches = R.launch_count() - l0
-        row = {"workload": c.name, "tokens": c.tokens, "launches_per_call": launches}
+        row = {"workload": c.name, "tokens": c.tokens, "launches_per_call": launches,
+               "host_us_per_call": host_us(enqueue), "host_us_per_prepared_call": host_us(prepared)}
         if launches == 0:  # the no-op: the call returns before any CUDA call
-            h0 = time.perf_counter()
-            for _ in range(1000):
-                enqueue()
-            row.update({"bytes_per_call": 0, "host_us_per_call": round((time.perf_counter() - h0) * 1e3, 3)})
+            row["bytes_per_call"] = 0
             rows.append(row)
             continue
         nbytes = algorithmic_bytes(c)

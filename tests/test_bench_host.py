@@ -95,3 +95,30 @@ def test_threaded_oracle_driver_is_bit_exact_with_one_thread():
 def test_host_cpu_description():
     h = bench.host_cpu()
     assert h["nproc"] >= 1 and 1 <= h["usable_cores"] <= h["nproc"] and h["cpu_model"]
+
+
+def test_small_call_workloads_and_their_bytes():
+    """The small-call table: the [1,16,2,64] f32 workload in its three variants,
+    then decode batches of every cache-op head layout and of the fused op."""
+    ws = bench.small_workloads()
+    names = [w.name for w in ws]
+    assert names[:3] == ["inplace_f32_1x16x2x64_slice16_48", "inplace_f32_1x16x2x64_slice0_0",
+                         "inplace_f32_1x16x2x64_slice8_8"]
+    assert bench.algorithmic_bytes(ws[0]) == 12288 and bench.algorithmic_bytes(ws[1]) == 24576
+    assert (ws[2].start, ws[2].end) == (8, 8)
+    for T in bench.DECODE_TOKENS:
+        neox = ws[names.index("decode_rope_neox_bf16_%dtok_32q8k_h128" % T)]
+        assert bench.algorithmic_bytes(neox) == T * (40 * 128 * 2 * 2 + 128 * 2 + 8)
+        gptj = ws[names.index("decode_rope_gptj_f16_%dtok_16q16k_h256_r64" % T)]
+        assert bench.algorithmic_bytes(gptj) == T * (32 * 64 * 2 * 2 + 64 * 2 + 8)
+        mrope = ws[names.index("decode_mrope_neox_bf16_%dtok_28q4k_h128_s16_24_24" % T)]
+        assert bench.algorithmic_bytes(mrope) == T * (32 * 128 * 2 * 2 + 128 * 2 + 3 * 8)
+        qkv = ws[names.index("decode_qkv_rmsnorm_rope_bf16_%dseq_32q8k8v_h128" % T)]
+        assert qkv.tokens == T and int((qkv.slot_mapping >= 0).sum()) == T
+
+
+def test_source_hash_ignores_comments_and_layout():
+    a = "int f(int x) {  // twice x\n  return 2 * x; /* done */ }\n"
+    b = "int f(int x) {\n/* a different comment */ return 2 *\n x; }"
+    assert bench.source_tokens(a) == bench.source_tokens(b)
+    assert bench.source_tokens(a) != bench.source_tokens(a.replace("2 * x", "3 * x"))
