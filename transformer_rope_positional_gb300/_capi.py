@@ -144,10 +144,15 @@ def _one_device(*tensors) -> int:
     return dev
 
 
+# the current device without the public call's lazy-initialisation check (CUDA
+# is initialised once CUDA tensors exist); the public call is the fallback
+_current_device = getattr(torch._C, "_cuda_getDevice", None) or torch.cuda.current_device
+
+
 def _on_device(dev: int, fn, args):
     """Call fn(*args) with device ``dev`` current (the library launches on the
     current device and sizes its grid from it)."""
-    if dev is None or dev < 0 or torch.cuda.current_device() == dev:
+    if dev is None or dev < 0 or _current_device() == dev:
         return fn(*args)
     with torch.cuda.device(dev):
         return fn(*args)
