@@ -36,6 +36,20 @@ int sm_count() {
   return g_sm_count[dev];
 }
 
+cudaError_t opt_in_shared(const void* kernel, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> granted;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = granted[std::make_pair(dev, kernel)];
+  if (have >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess) have = smem;
+  return e;
+}
+
 int resident_blocks(const void* kernel, int threads, size_t smem) {
   static std::mutex mu;
   static std::map<std::tuple<int, const void*, int, size_t>, int> cache;

@@ -216,6 +216,42 @@ __device__ __forceinline__ void load_f32(float (&out)[N], const T* p, const Span
   }
 }
 
+// ---------------------------------------------------------------------------
+// Asynchronous 16-byte global -> shared copies (cp.async, cached in L2 only,
+// evict-first there), completed in commit groups.  A thread that copies into
+// a shared-memory slot and later reads that slot itself needs only
+// cp_async_wait(), no barrier.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, uint64_t policy) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's commit groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The copy with the bounds check of access_ok() (a skipped copy leaves zeros).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, uint64_t policy, const Span& s,
+                                           unsigned int* err) {
+  if (access_ok(gmem, 16, s, err)) {
+    cp_async16(smem, gmem, policy);
+  } else {
+    *static_cast<uint4*>(smem) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // Scalar read-only load (zero when a debug build skips it).
 template <typename T>
 __device__ __forceinline__ T ldg(const T* p, const Span& s, unsigned int* err) {

@@ -93,6 +93,9 @@ int sm_count();
 // dynamic shared memory) that fit on one SM of the current device; cached, at
 // least 1.
 int resident_blocks(const void* kernel, int threads, size_t smem = 0);
+// Let `kernel` launch with `smem` bytes of dynamic shared memory on the current
+// device (needed above 48 KB); remembered per device and kernel.
+cudaError_t opt_in_shared(const void* kernel, size_t smem);
 
 // Launch `kernel` on `stream` with programmatic stream serialization allowed:
 // the kernel may be scheduled while the previous kernel of the stream drains,

@@ -18,7 +18,16 @@
 //
 //  * RMSNorm: each thread sums the squares of its 2*VEC elements, then a
 //    butterfly of warp shuffles inside the row group (padded to a power of two
-//    lanes) completes the head's sum; a head never leaves registers.
+//    lanes) completes the head's sum.
+//  * Head rows through shared memory: each thread copies its 16-byte chunks of
+//    the NEXT item's rows into shared-memory slots of its own with cp.async
+//    (cached in L2 only, evict-first) before it works on the current item,
+//    whose rows arrived meanwhile, so a whole item of reads stays in flight
+//    while the thread computes; no barrier is needed, since a thread reads
+//    back only its own slots.  Two buffers measured best (35.9 -> 34.9 us on
+//    the mixed prefill/decode batch); three or four buffers, reading the rows
+//    from shared memory again for the rotation, and 5 CTAs per SM (which
+//    spills) were slower.
 //  * RoPE with the norm folded in: per item, thread c forms the products
 //    gamma_low*cos, -gamma_high*sin, gamma_high*cos, gamma_low*sin of its
 //    elements once, so each output element costs one product, one FMA and
@@ -51,11 +60,21 @@ namespace {
 #ifndef ROPE_QKV_MIN_BLOCKS
 #define ROPE_QKV_MIN_BLOCKS 4
 #endif
+// Row buffers per thread: the current item plus ROPE_QKV_STAGES - 1 items
+// whose rows are being copied (2 measured best: 3 and 4 were slower).
+#ifndef ROPE_QKV_STAGES
+#define ROPE_QKV_STAGES 2
+#endif
 constexpr int kRowsInFlight = ROPE_QKV_ROWS_IN_FLIGHT;
+constexpr int kStages = ROPE_QKV_STAGES;
+
+static_assert(kStages >= 2, "at least one item in flight");
 constexpr int kThreads = ROPE_QKV_THREADS;
 constexpr unsigned kPositionOutOfRange = 1u;
 constexpr unsigned kSlotOutOfRange = 2u;
 constexpr int64_t kSharedTable = 4096;  // int64 entries of the shared batch tables (32 KB)
+// Row stages: [kStages buffers][U rows][2 halves][kThreads] 16-byte slots.
+constexpr size_t kStageBytes = size_t(kStages) * kRowsInFlight * 2 * kThreads * 16;
 
 struct QkvArgs {
   int64_t T, B;
@@ -104,6 +123,27 @@ __device__ __forceinline__ int find_batch(const int64_t* __restrict__ qsl, int B
   return lo;
 }
 
+// The heads of item index r within its token: kind 0 q, 1 k, 2 v; h0 the
+// first head within the kind, n heads, hg the first head within the qkv row.
+struct ItemHeads {
+  int kind, h0, n, hg;
+};
+
+__device__ __forceinline__ ItemHeads item_heads(int r, const QkvArgs& a) {
+  constexpr int U = kRowsInFlight;
+  ItemHeads h;
+  int nh;
+  if (r < a.iq) {
+    h.kind = 0, h.h0 = r * U, nh = a.nq, h.hg = h.h0;
+  } else if (r < a.iq + a.ik) {
+    h.kind = 1, h.h0 = (r - a.iq) * U, nh = a.nk, h.hg = a.nq + h.h0;
+  } else {
+    h.kind = 2, h.h0 = (r - a.iq - a.ik) * U, nh = a.nv, h.hg = a.nq + a.nk + h.h0;
+  }
+  h.n = min(U, nh - h.h0);
+  return h;
+}
+
 template <bool SHARED>
 __device__ __forceinline__ ItemMeta item_meta(int64_t item, const QkvArgs& a, const int64_t* __restrict__ tab,
                                               const int64_t* __restrict__ qsl, const int64_t* __restrict__ seq_lens,
@@ -142,8 +182,38 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
   const int i0 = (active ? c : 0) * VEC;
   wait_for_prior_grid();
 
-  // [0, B]: queryStartLoc; [B + 1, 2B]: seqLens[b] - queryStartLoc[b + 1]
-  extern __shared__ int64_t s_tab[];
+  extern __shared__ __align__(16) unsigned char s_raw[];
+  // row stages, then [0, B]: queryStartLoc; [B + 1, 2B]: seqLens[b] - queryStartLoc[b + 1]
+  uint4* const s_stage = reinterpret_cast<uint4*>(s_raw);
+  int64_t* const s_tab = reinterpret_cast<int64_t*>(s_raw + kStageBytes);
+  auto slot = [&](int buf, int u, int v) { return s_stage + ((buf * U + u) * 2 + v) * kThreads + threadIdx.x; };
+  const uint64_t policy = l2_evict_first_policy();
+  // copies of item `it`'s head rows into buffer `buf`, as one commit group
+  auto copy_rows = [&](int64_t it, int buf) {
+    if (active) {
+      const int64_t t = div_index(it, a.per_token, a.items32);
+      const ItemHeads hd = item_heads((int)(it - t * a.per_token), a);
+      const T* src = qkv + t * a.W + (int64_t)hd.hg * a.D + i0;
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (u < hd.n) {
+          cp_async16(slot(buf, u, 0), src + u * a.D, policy, a.qkv_span, err);
+          cp_async16(slot(buf, u, 1), src + u * a.D + half, policy, a.qkv_span, err);
+        }
+    }
+    cp_async_commit();
+  };
+
+  const int64_t stride = (int64_t)gridDim.x * P;
+  int64_t item = (int64_t)blockIdx.x * P + g;
+  int buf = 0;  // buffer of the current item; item + j * stride goes to (buf + j) % kStages
+  // the first items' rows are copied before the tables are built: they need no metadata
+#pragma unroll
+  for (int j = 0; j < kStages - 1; ++j) {
+    if (item + j * stride < a.items) copy_rows(item + j * stride, j);
+    else cp_async_commit();
+  }
+
 #ifdef ROPE_DEBUG_BOUNDS
   a.tab_span.lo = reinterpret_cast<const char*>(s_tab);
   a.tab_span.hi = reinterpret_cast<const char*>(s_tab + (SHARED ? 2 * a.B + 1 : 0));
@@ -155,21 +225,19 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
     __syncthreads();
   }
 
-  const int64_t stride = (int64_t)gridDim.x * P;
-  int64_t item = (int64_t)blockIdx.x * P + g;
   if (item >= a.items) return;
   ItemMeta m = item_meta<SHARED>(item, a, s_tab, qsl, seq_lens, slot_mapping, 0, err);
   for (; item < a.items; item += stride) {
-    // ---- this item's heads: kind 0 q, 1 k, 2 v; h0 within the kind
-    int kind, h0, nh, hg;
-    if (m.r < a.iq) {
-      kind = 0, h0 = m.r * U, nh = a.nq, hg = h0;
-    } else if (m.r < a.iq + a.ik) {
-      kind = 1, h0 = (m.r - a.iq) * U, nh = a.nk, hg = a.nq + h0;
-    } else {
-      kind = 2, h0 = (m.r - a.iq - a.ik) * U, nh = a.nv, hg = a.nq + a.nk + h0;
+    const int64_t next = item + stride;
+    {
+      const int64_t ahead = item + (kStages - 1) * stride;
+      const int abuf = buf == 0 ? kStages - 1 : buf - 1;  // (buf + kStages - 1) % kStages
+      if (ahead < a.items) copy_rows(ahead, abuf);
+      else cp_async_commit();  // one group per item keeps the wait count fixed
     }
-    const int n = min(U, nh - h0);
+    // ---- this item's heads: kind 0 q, 1 k, 2 v; h0 within the kind
+    const ItemHeads hd = item_heads(m.r, a);
+    const int kind = hd.kind, h0 = hd.h0, n = hd.n;
     const bool pos_ok = m.position >= 0 && m.position < a.max_seq;
     const bool cache_it = m.slot >= 0 && m.slot < a.num_slots;
     const bool work = pos_ok && (kind == 0 || cache_it);  // uniform over the row group
@@ -178,13 +246,6 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
     Vec<T, VEC> x1[U], x2[U];
     Vec<T, VEC> cv, sv, g1, g2;
     if (work && active) {
-      const T* src = qkv + m.t * a.W + (int64_t)hg * a.D + i0;
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (u < n) {
-          load_vec<true>(x1[u], src + u * a.D, a.qkv_span, err);
-          load_vec<true>(x2[u], src + u * a.D + half, a.qkv_span, err);
-        }
       if (rotate) {
         const T* cs = cache + m.position * a.D + i0;
         load_vec<false>(cv, cs, a.cache_span, err);
@@ -213,9 +274,20 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
       dstride = (int64_t)a.block_size * a.D;
     }
     // ---- next item's metadata while the loads are in flight
-    const int64_t next = item + stride;
     const ItemMeta mn =
         next < a.items ? item_meta<SHARED>(next, a, s_tab, qsl, seq_lens, slot_mapping, m.b, err) : m;
+    {  // this item's rows, copied kStages - 1 items ago
+      cp_async_wait<kStages - 1>();
+      if (work && active) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (u < n) {
+            *reinterpret_cast<uint4*>(x1[u].e) = *slot(buf, u, 0);
+            *reinterpret_cast<uint4*>(x2[u].e) = *slot(buf, u, 1);
+          }
+      }
+      buf = buf + 1 == kStages ? 0 : buf + 1;
+    }
 
     if (work && rotate) {
       // RMSNorm: squares of every row of the item (independent chains), then
@@ -287,8 +359,14 @@ cudaError_t launch_tables(const QkvProblem& p, const QkvArgs& a, cudaStream_t st
   constexpr int VEC = 16 / sizeof(T);
   const int64_t groups = kThreads / a.group;
   auto kernel = qkv_kernel<T, VEC, SHARED>;
-  // shared tables rounded up to 4 KB so that few distinct sizes reach the occupancy cache
-  const size_t smem = SHARED ? (size_t)((2 * p.B + 1) * sizeof(int64_t) + 4095) / 4096 * 4096 : 0;
+  // row stages, then the shared tables rounded up to 4 KB so that few distinct
+  // sizes reach the occupancy cache
+  const size_t tables = SHARED ? (size_t)((2 * p.B + 1) * sizeof(int64_t) + 4095) / 4096 * 4096 : 0;
+  const size_t smem = kStageBytes + tables;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = opt_in_shared(reinterpret_cast<const void*>(kernel), smem);
+    if (e != cudaSuccess) return e;
+  }
   const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), kThreads, smem);
   const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
   unsigned int* err = nullptr;
