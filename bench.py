@@ -200,13 +200,19 @@ def source_tokens(text: str) -> str:
     return " ".join(text.split())
 
 
+# The C ABI's argument checks: host code that runs before any launch and
+# changes neither a kernel nor its launch configuration.
+ARGUMENT_CHECKS = "rope_api.cu"
+
+
 def kernel_source_hash() -> str:
-    """sha256[:16] of the kernel sources' code (comments and layout excluded),
-    so that a profile stays tied to the code it measured."""
+    """sha256[:16] of the kernel sources' code (comments and layout excluded):
+    the kernels, their launchers and launch bookkeeping, not the argument
+    checks; so that a profile stays tied to the code it measured."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transformer_rope_positional_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cu", ".cuh", ".h")) and name != ARGUMENT_CHECKS:
             with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 h.update(name.encode() + b"\0" + source_tokens(f.read()).encode())
     return h.hexdigest()[:16]

@@ -29,13 +29,21 @@
  * Arithmetic.  Half-precision inputs are widened to binary32; each output is
  * a two-term dot product evaluated with Kahan's FMA-based difference of
  * products (relative error <= 2^-23, see Jeannerod, Louvet & Muller, Math. Comp.
- * 82 (2013)) and rounded once, to nearest even, to the output type.  Results
- * are deterministic and do not depend on the launch shape.
+ * 82 (2013)) and rounded once, to nearest even, to the output type.  Where
+ * both products are exact in binary32 (query, key and the cache all binary16,
+ * or all bfloat16, in the GPT-J and out-of-place cache kernels) it is one FMA
+ * after an exact product: the correctly rounded binary32 value.  Results are
+ * deterministic and do not depend on the launch shape.
  *
  * Errors.  Every argument check happens on the host before anything is
  * enqueued; a failed check returns a status and enqueues nothing.  A shape
  * whose element count (or a strided view's extent) overflows, or exceeds
- * INT64_MAX / 8, is ROPE_ERR_PARAM_INVALID.  Status
+ * INT64_MAX / 8, is ROPE_ERR_PARAM_INVALID.  So is a tensor the call rewrites
+ * that shares memory with a tensor it reads or another one it writes (x with
+ * cos or sin; in place, query with key, positions or the cache; an output of
+ * the fused op with any other tensor of the call), whose result would depend
+ * on the order in which threads run; query and key as disjoint column ranges
+ * of one buffer, with one row stride, are accepted.  Status
  * values 161001 and 161002 are the ones [IPRM §返回值与错误码] lists
  * (ACLNN_ERR_PARAM_NULLPTR, ACLNN_ERR_PARAM_INVALID).  A CUDA launch error is
  * returned as ROPE_ERR_CUDA; errors that happen while the work runs surface at

@@ -122,3 +122,18 @@ def test_source_hash_ignores_comments_and_layout():
     b = "int f(int x) {\n/* a different comment */ return 2 *\n x; }"
     assert bench.source_tokens(a) == bench.source_tokens(b)
     assert bench.source_tokens(a) != bench.source_tokens(a.replace("2 * x", "3 * x"))
+
+
+def test_the_unhashed_argument_checks_hold_no_kernel_or_launch():
+    """The profile hash leaves out the C ABI's argument checks; that file must
+    stay host-only code that neither defines nor launches a kernel, nor sizes a
+    launch, or a change there could alter what the profiles measured."""
+    path = os.path.join(os.path.dirname(bench.__file__), "transformer_rope_positional_gb300", "csrc",
+                        bench.ARGUMENT_CHECKS)
+    code = bench.source_tokens(open(path).read())
+    for marker in ("__global__", "__device__", "<<<", "cudaLaunch", "resident_blocks", "sm_count", "opt_in_shared",
+                   "cudaFuncSetAttribute", "__launch_bounds__"):
+        assert marker not in code, marker
+    csrc = os.path.dirname(path)
+    hashed = [n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")) and n != bench.ARGUMENT_CHECKS]
+    assert {"rope_cache.cu", "rope_qkv.cu", "rope_launch.cu", "rope_inplace.cuh", "rope_device.cuh"} <= set(hashed)

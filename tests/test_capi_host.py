@@ -349,3 +349,58 @@ def test_shapes_whose_element_count_overflows_are_refused(lib):
     assert _qkv(lib, nq=4, nk=0, nv=0, qkv=_d(C.BF16, (6, 4 * 64)), qo=_d(C.BF16, (6, 4 * 64)),
                 kc=_d(C.BF16, (big, 0, 1 << 30, 64)), vc=_d(C.BF16, (big, 0, 1 << 30, 64))) \
         == C.ROPE_ERR_PARAM_INVALID
+
+
+# ---------------------------------------------------------------------------
+# Aliasing: a tensor the call rewrites must not share memory with one it reads
+# (the result would depend on the order in which threads run).  Only
+# rejections are tested here: an accepted call would launch.
+# ---------------------------------------------------------------------------
+MB = 1 << 20  # distinct tensors sit MB apart
+
+
+@pytest.mark.parametrize("cos_at,sin_at", [(FAKE + 256, FAKE + MB), (FAKE + MB, FAKE + 1024), (FAKE, FAKE)])
+def test_inplace_x_sharing_memory_with_cos_or_sin_is_rejected(lib, cos_at, sin_at):
+    x = _d(C.F32, X, FAKE)  # 6 KB
+    assert _inplace(lib, x, _d(C.F32, CS, cos_at), _d(C.F32, CS, sin_at)) == C.ROPE_ERR_PARAM_INVALID
+
+
+@pytest.mark.parametrize("q_at,k_at,p_at,c_at", [
+    (FAKE, FAKE, FAKE + 4 * MB, FAKE + 8 * MB),             # query and key the same buffer
+    (FAKE, FAKE + 512, FAKE + 4 * MB, FAKE + 8 * MB),       # key starts inside query
+    (FAKE, FAKE + 2 * MB, FAKE + 1024, FAKE + 8 * MB),      # positions inside query
+    (FAKE, FAKE + 2 * MB, FAKE + 4 * MB, FAKE + 2 * MB + 64),  # the cache inside key
+])
+def test_cache_rewritten_rows_sharing_memory_are_rejected(lib, q_at, k_at, p_at, c_at):
+    _, q, k, c = good()
+    pos = _d(C.I64, (T,), p_at)
+    q, k, c = _d(q.dtype, tuple(q.shape[:2]), q_at), _d(k.dtype, tuple(k.shape[:2]), k_at), \
+        _d(c.dtype, tuple(c.shape[:2]), c_at)
+    assert _cache(lib, pos, q, k, c) == C.ROPE_ERR_PARAM_INVALID
+
+
+def test_cache_row_views_whose_columns_collide_are_rejected(lib):
+    # q and k as row views of one [T, 3 * 256] buffer: k's columns [128, 384)
+    # cross q's [0, 256); the disjoint layout ([256, 384)) is what fused QKV
+    # buffers use and is exercised on the GPU
+    W = 3 * 256
+    q = _d(C.BF16, (T, 256), FAKE)
+    k = _d(C.BF16, (T, 128), FAKE + 128 * 2)
+    assert _v2(lib, _d(C.I64, (T,), FAKE + 4 * MB), q, k, _d(C.BF16, (100, 64), FAKE + 8 * MB), qs=W,
+               ks=W) == C.ROPE_ERR_PARAM_INVALID
+
+
+@pytest.mark.parametrize("over", [
+    dict(qo=_d(C.BF16, (6, 2 * 64), 1 * MB + 1024)),      # q_out inside qkv
+    dict(vc=_d(C.BF16, (3, 1, 4, 64), 12 * MB)),          # v_cache is k_cache
+    dict(kc=_d(C.BF16, (3, 1, 4, 64), 10 * MB + 512)),    # k_cache over q_out
+    dict(slots=_d(C.I64, (6,), 12 * MB + 8)),             # slot_mapping inside k_cache
+], ids=["q_out_in_qkv", "v_cache_is_k_cache", "k_cache_over_q_out", "slots_in_k_cache"])
+def test_qkv_outputs_sharing_memory_are_rejected(lib, over):
+    D = 64
+    t = dict(qkv=_d(C.BF16, (6, 4 * D), 1 * MB), qg=_d(C.BF16, (D,), 2 * MB), kg=_d(C.BF16, (D,), 3 * MB),
+             cache=_d(C.BF16, (50, D), 4 * MB), sl=_d(C.I64, (2,), 5 * MB), qsl=_d(C.I64, (3,), 6 * MB),
+             slots=_d(C.I64, (6,), 7 * MB), qo=_d(C.BF16, (6, 2 * D), 10 * MB),
+             kc=_d(C.BF16, (3, 1, 4, D), 12 * MB), vc=_d(C.BF16, (3, 1, 4, D), 13 * MB))
+    t.update(over)
+    assert _qkv(lib, **t) == C.ROPE_ERR_PARAM_INVALID

@@ -29,7 +29,8 @@ LIB_DIR = os.path.join(HERE, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "librope_gb300.so")
 DEBUG_LIB_PATH = os.path.join(LIB_DIR, "librope_gb300_debug.so")
 
-SOURCES = ["rope_api.cu", "rope_inplace_fwd.cu", "rope_inplace_bwd.cu", "rope_cache.cu", "rope_qkv.cu"]
+SOURCES = ["rope_api.cu", "rope_launch.cu", "rope_inplace_fwd.cu", "rope_inplace_bwd.cu", "rope_cache.cu",
+           "rope_qkv.cu"]
 HEADERS = ["rope_device.cuh", "rope_launch.h", "rope_inplace.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]

@@ -6,72 +6,11 @@
 // RopeWithSinCosCache 深度解析…", sections 约束说明 and 入参校验逻辑).  Every check
 // runs on the host before anything is enqueued, and no check touches the GPU,
 // so a rejected call has no side effect at all.
-#include <atomic>
-#include <map>
-#include <mutex>
-#include <tuple>
+#include <initializer_list>
 
 #include "rope_gb300.h"
 #include "rope_launch.h"
 
-namespace rope {
-
-namespace {
-std::atomic<uint64_t> g_launches{0};
-constexpr int kMaxDevices = 64;
-std::once_flag g_sm_once[kMaxDevices];
-int g_sm_count[kMaxDevices];
-}  // namespace
-
-void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
-
-int sm_count() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-  std::call_once(g_sm_once[dev], [dev] {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    g_sm_count[dev] = n;
-  });
-  return g_sm_count[dev];
-}
-
-cudaError_t opt_in_shared(const void* kernel, size_t smem) {
-  static std::mutex mu;
-  static std::map<std::pair<int, const void*>, size_t> granted;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lock(mu);
-  size_t& have = granted[std::make_pair(dev, kernel)];
-  if (have >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e == cudaSuccess) have = smem;
-  return e;
-}
-
-int resident_blocks(const void* kernel, int threads, size_t smem) {
-  static std::mutex mu;
-  static std::map<std::tuple<int, const void*, int, size_t>, int> cache;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
-  const auto key = std::make_tuple(dev, kernel, threads, smem);
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) return it->second;
-  }
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) {
-    (void)cudaGetLastError();  // do not leave a sticky-looking error for the launch check
-    n = 1;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  cache[key] = n;
-  return n;
-}
-
-}  // namespace rope
 
 namespace {
 
@@ -117,6 +56,35 @@ int64_t strided_extent(int64_t rows, int64_t stride, int64_t width) {
 
 bool aligned(const void* p, uintptr_t bytes) { return reinterpret_cast<uintptr_t>(p) % bytes == 0; }
 
+int64_t elem_size(int32_t dt) { return dt == kF32 ? 4 : dt == kI64 ? 8 : 2; }
+
+// Whether two sets of `rows` rows share a byte: set a starts at byte address
+// a, its rows are aw bytes wide and as bytes apart (likewise b).  Sets whose
+// byte ranges meet are treated as overlapping unless both have one stride s
+// and their columns are disjoint modulo s (e.g. the q and k column ranges of
+// one fused QKV buffer).  Empty sets overlap nothing.
+bool rows_overlap(uintptr_t a, int64_t as, int64_t aw, uintptr_t b, int64_t bs, int64_t bw, int64_t rows) {
+  if (rows <= 0 || aw <= 0 || bw <= 0) return false;
+  const uintptr_t a_end = a + (uintptr_t)((rows - 1) * as + aw), b_end = b + (uintptr_t)((rows - 1) * bs + bw);
+  if (a_end <= b || b_end <= a) return false;
+  if (rows == 1 || as != bs || aw > as || bw > bs) return true;
+  // a covers [0, aw) of every period of as bytes, b covers [r, r + bw)
+  const int64_t d = (int64_t)(b - a);
+  const int64_t r = ((d % as) + as) % as;
+  return r < aw || r + bw > as;
+}
+
+// Whether the byte ranges [a, a + an) and [b, b + bn) share a byte.
+bool ranges_overlap(uintptr_t a, int64_t an, uintptr_t b, int64_t bn) {
+  return an > 0 && bn > 0 && a < b + (uintptr_t)bn && b < a + (uintptr_t)an;
+}
+
+// Whether two contiguous tensors (the byte ranges of their elements) overlap.
+bool tensors_overlap(const rope_tensor_t* x, const rope_tensor_t* y) {
+  return ranges_overlap(reinterpret_cast<uintptr_t>(x->data), numel(x) * elem_size(x->dtype),
+                        reinterpret_cast<uintptr_t>(y->data), numel(y) * elem_size(y->dtype));
+}
+
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? ROPE_OK : ROPE_ERR_CUDA; }
 
 // Checks shared by the forward and backward in-place calls, then the launch.
@@ -146,6 +114,8 @@ int inplace_call(const rope_tensor_t* x, const rope_tensor_t* cos, const rope_te
   if (!x->data || !cos->data || !sin->data) return ROPE_ERR_PARAM_NULLPTR;
   const uintptr_t xe = x->dtype == kF32 ? 4 : 2, ce = cos->dtype == kF32 ? 4 : 2;
   if (!aligned(x->data, xe) || !aligned(cos->data, ce) || !aligned(sin->data, ce)) return ROPE_ERR_PARAM_INVALID;
+  // x is rewritten while cos/sin are read: they must not share memory
+  if (tensors_overlap(x, cos) || tensors_overlap(x, sin)) return ROPE_ERR_PARAM_INVALID;
 
   rope::InplaceProblem p;
   p.mode = (int32_t)rotary_mode;
@@ -238,6 +208,18 @@ int cache_call(const rope_tensor_t* positions, const rope_tensor_t* query, const
   bool in_place = query_out == nullptr;
   if (!in_place && query_out->data == query->data && key_out->data == key->data && qs == qw && ks == kw)
     in_place = true;
+  {
+    // rewritten rows must not share memory with each other or with the tables
+    const uintptr_t qa = reinterpret_cast<uintptr_t>(query->data), ka = reinterpret_cast<uintptr_t>(key->data);
+    const int64_t pb = numel(positions) * 8, cb = numel(cos_sin_cache) * esz;
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(positions->data),
+                    ca = reinterpret_cast<uintptr_t>(cos_sin_cache->data);
+    const int64_t qn = ((T - 1) * qs + qw) * esz, kn = ((T - 1) * ks + kw) * esz;
+    if (in_place && (rows_overlap(qa, qs * esz, qw * esz, ka, ks * esz, kw * esz, T) ||
+                     ranges_overlap(qa, qn, pa, pb) || ranges_overlap(qa, qn, ca, cb) ||
+                     ranges_overlap(ka, kn, pa, pb) || ranges_overlap(ka, kn, ca, cb)))
+      return ROPE_ERR_PARAM_INVALID;
+  }
   if (!in_place) {
     const char* spans[4][2] = {
         {static_cast<const char*>(query->data), static_cast<const char*>(query->data) + ((T - 1) * qs + qw) * esz},
@@ -318,6 +300,11 @@ int qkv_call(const rope_tensor_t* qkv, int64_t nq, int64_t nk, int64_t nv, const
   if (!(eps >= 0.0f) || !(eps < 1e30f)) return ROPE_ERR_PARAM_INVALID;
   for (const rope_tensor_t* t : all)
     if (!t->data && numel(t) > 0) return ROPE_ERR_PARAM_NULLPTR;
+  // the outputs are written while every input is read: no output may share
+  // memory with an input or with another output
+  for (const rope_tensor_t* o : {q_out, k_cache, v_cache})
+    for (const rope_tensor_t* t : all)
+      if (t != o && tensors_overlap(o, t)) return ROPE_ERR_PARAM_INVALID;
   for (const rope_tensor_t* t : {qkv, q_gamma, k_gamma, cache, q_out, k_cache, v_cache})
     if (t->data && !aligned(t->data, 16)) return ROPE_ERR_PARAM_INVALID;
   for (const rope_tensor_t* t : {seq_lens, qsl, slot_mapping})
@@ -413,7 +400,7 @@ const char* rope_status_string(int status) {
   }
 }
 
-uint64_t rope_launch_count(void) { return rope::g_launches.load(std::memory_order_relaxed); }
+uint64_t rope_launch_count(void) { return rope::launch_count(); }
 
 int rope_abi_version(void) { return ROPE_ABI_VERSION; }
 

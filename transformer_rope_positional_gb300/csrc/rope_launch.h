@@ -88,6 +88,7 @@ cudaError_t device_error_address(unsigned int** out);
 
 // Launch bookkeeping.
 void count_launch();
+uint64_t launch_count();
 int sm_count();
 // CTAs of `kernel` (launched with `threads` threads and `smem` bytes of
 // dynamic shared memory) that fit on one SM of the current device; cached, at
