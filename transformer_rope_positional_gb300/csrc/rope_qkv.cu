@@ -91,6 +91,9 @@ struct QkvArgs {
   int32_t group;        // C rounded up to a power of two (lanes per row group)
   float eps;
   float inv_d;
+  int64_t stride_t;     // a row group's step of grid * groups items: whole tokens
+  int32_t stride_r;     // and items left over (< per_token)
+  int32_t bs_shift;     // log2(block_size) when it is a power of two, else -1
   bool items32;  // items and slots fit 32-bit index arithmetic
   // byte spans of the tensors (checked in debug builds)
   Span qkv_span, qg_span, kg_span, cache_span, sl_span, qsl_span, slot_span, qo_span, kc_span, vc_span, tab_span;
@@ -144,14 +147,27 @@ __device__ __forceinline__ ItemHeads item_heads(int r, const QkvArgs& a) {
   return h;
 }
 
+// Item index as (token, item within the token), stepped by the grid stride
+// without a division.
+struct TokenItem {
+  int64_t t;
+  int32_t r;
+};
+
+__device__ __forceinline__ void advance(TokenItem& ti, const QkvArgs& a) {
+  ti.t += a.stride_t;
+  ti.r += a.stride_r;
+  if (ti.r >= a.per_token) ti.r -= a.per_token, ++ti.t;
+}
+
 template <bool SHARED>
-__device__ __forceinline__ ItemMeta item_meta(int64_t item, const QkvArgs& a, const int64_t* __restrict__ tab,
+__device__ __forceinline__ ItemMeta item_meta(TokenItem ti, const QkvArgs& a, const int64_t* __restrict__ tab,
                                               const int64_t* __restrict__ qsl, const int64_t* __restrict__ seq_lens,
                                               const int64_t* __restrict__ slot_mapping, int cursor,
                                               unsigned int* err) {
   ItemMeta m;
-  m.t = div_index(item, a.per_token, a.items32);
-  m.r = (int32_t)(item - m.t * a.per_token);
+  m.t = ti.t;
+  m.r = ti.r;
   m.slot = ldg(slot_mapping + m.t, a.slot_span, err);
   if (SHARED) {
     m.b = find_batch(tab, (int)a.B, m.t, cursor, a.tab_span, err);
@@ -189,11 +205,10 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
   auto slot = [&](int buf, int u, int v) { return s_stage + ((buf * U + u) * 2 + v) * kThreads + threadIdx.x; };
   const uint64_t policy = l2_evict_first_policy();
   // copies of item `it`'s head rows into buffer `buf`, as one commit group
-  auto copy_rows = [&](int64_t it, int buf) {
+  auto copy_rows = [&](const TokenItem& it, int buf) {
     if (active) {
-      const int64_t t = div_index(it, a.per_token, a.items32);
-      const ItemHeads hd = item_heads((int)(it - t * a.per_token), a);
-      const T* src = qkv + t * a.W + (int64_t)hd.hg * a.D + i0;
+      const ItemHeads hd = item_heads(it.r, a);
+      const T* src = qkv + it.t * a.W + (int64_t)hd.hg * a.D + i0;
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (u < hd.n) {
@@ -204,14 +219,20 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
     cp_async_commit();
   };
 
-  const int64_t stride = (int64_t)gridDim.x * P;
-  int64_t item = (int64_t)blockIdx.x * P + g;
-  int buf = 0;  // buffer of the current item; item + j * stride goes to (buf + j) % kStages
+  // items in token order: item i is (token i / per_token, item i % per_token
+  // within it); a row group steps by the grid's groups, in (token, item) form
+  const int64_t item0 = (int64_t)blockIdx.x * P + g;
+  int buf = 0;  // buffer of the current item; the j-th item after it goes to (buf + j) % kStages
+  TokenItem tc;  // the current item (tc.t < T while there is one)
+  tc.t = div_index(item0, a.per_token, a.items32);
+  tc.r = (int32_t)(item0 - tc.t * a.per_token);
+  TokenItem ta = tc;  // the item whose rows are copied next
   // the first items' rows are copied before the tables are built: they need no metadata
 #pragma unroll
   for (int j = 0; j < kStages - 1; ++j) {
-    if (item + j * stride < a.items) copy_rows(item + j * stride, j);
+    if (ta.t < a.T) copy_rows(ta, j);
     else cp_async_commit();
+    advance(ta, a);
   }
 
 #ifdef ROPE_DEBUG_BOUNDS
@@ -225,15 +246,17 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
     __syncthreads();
   }
 
-  if (item >= a.items) return;
-  ItemMeta m = item_meta<SHARED>(item, a, s_tab, qsl, seq_lens, slot_mapping, 0, err);
-  for (; item < a.items; item += stride) {
-    const int64_t next = item + stride;
+  if (tc.t >= a.T) return;
+  ItemMeta m = item_meta<SHARED>(tc, a, s_tab, qsl, seq_lens, slot_mapping, 0, err);
+  for (;;) {  // m: the current item's metadata, m.t < T
+    TokenItem tn = {m.t, m.r};  // the next item
+    advance(tn, a);
     {
-      const int64_t ahead = item + (kStages - 1) * stride;
       const int abuf = buf == 0 ? kStages - 1 : buf - 1;  // (buf + kStages - 1) % kStages
-      if (ahead < a.items) copy_rows(ahead, abuf);
+      if (kStages == 2) ta = tn;  // the item kStages - 1 ahead is the next one
+      if (ta.t < a.T) copy_rows(ta, abuf);
       else cp_async_commit();  // one group per item keeps the wait count fixed
+      if (kStages > 2) advance(ta, a);
     }
     // ---- this item's heads: kind 0 q, 1 k, 2 v; h0 within the kind
     const ItemHeads hd = item_heads(m.r, a);
@@ -267,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
     if (kind == 0) {
       dst = q_out + (m.t * a.nq + h0) * (int64_t)a.D;
     } else if (cache_it) {
-      const int64_t blk = div_index(m.slot, a.block_size, a.items32);
+      const int64_t blk = a.bs_shift >= 0 ? m.slot >> a.bs_shift : div_index(m.slot, a.block_size, a.items32);
       const int64_t off = m.slot - blk * a.block_size;
       dst = (kind == 1 ? k_cache + ((blk * a.nk + h0) * a.block_size + off) * a.D
                        : v_cache + ((blk * a.nv + h0) * a.block_size + off) * a.D);
@@ -275,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
     }
     // ---- next item's metadata while the loads are in flight
     const ItemMeta mn =
-        next < a.items ? item_meta<SHARED>(next, a, s_tab, qsl, seq_lens, slot_mapping, m.b, err) : m;
+        tn.t < a.T ? item_meta<SHARED>(tn, a, s_tab, qsl, seq_lens, slot_mapping, m.b, err) : m;
     {  // this item's rows, copied kStages - 1 items ago
       cp_async_wait<kStages - 1>();
       if (work && active) {
@@ -350,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, ROPE_QKV_MIN_BLOCKS)
           store_vec(dst + u * dstride + half + i0, x2[u], *dspan, err);
         }
     }
+    if (tn.t >= a.T) break;
     m = mn;
   }
 }
@@ -369,6 +393,9 @@ cudaError_t launch_tables(const QkvProblem& p, const QkvArgs& a, cudaStream_t st
   }
   const int64_t resident = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), kThreads, smem);
   const int64_t grid = std::max<int64_t>(1, std::min((a.items + groups - 1) / groups, resident));
+  QkvArgs args = a;
+  args.stride_t = grid * groups / a.per_token;
+  args.stride_r = (int32_t)(grid * groups % a.per_token);
   unsigned int* err = nullptr;
   const cudaError_t e = device_error_address(&err);
   if (e != cudaSuccess) return e;
@@ -376,7 +403,7 @@ cudaError_t launch_tables(const QkvProblem& p, const QkvArgs& a, cudaStream_t st
                                 static_cast<const T*>(p.q_gamma), static_cast<const T*>(p.k_gamma),
                                 static_cast<const T*>(p.cache), p.seq_lens, p.query_start_loc, p.slot_mapping,
                                 static_cast<T*>(p.q_out), static_cast<T*>(p.k_cache), static_cast<T*>(p.v_cache),
-                                err, a);
+                                err, args);
 }
 
 template <typename T>
@@ -404,6 +431,11 @@ cudaError_t launch_typed(const QkvProblem& p, cudaStream_t stream) {
   a.eps = p.eps;
   a.inv_d = 1.0f / (float)p.D;
   a.items32 = a.items <= 0xffffffffLL && a.num_slots <= 0xffffffffLL;
+  a.bs_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if ((int64_t(1) << sh) == p.block_size) a.bs_shift = sh;
+  a.stride_t = 0;  // set with the grid
+  a.stride_r = 0;
   const int64_t e = sizeof(T);
   a.qkv_span = make_span(p.qkv, p.T * a.W * e);
   a.qg_span = make_span(p.q_gamma, p.D * e);
