@@ -237,6 +237,15 @@ def recorded_traffic(label: str):
 # our arm
 # ----------------------------------------------------------------------------
 
+def step_config(total_bytes: int, step_tokens: int) -> dict:
+    """The ``config`` of the bench line, the same for both arms: the step's
+    workload, its algorithmic bytes and tokens, the L2 rule and the parallelism."""
+    return {"workload": WORKLOAD_NAME, "bytes_per_step": total_bytes, "tokens_per_step": step_tokens,
+            "l2": "inputs larger than L2: %.2f GB per step vs %d MB L2; each kernel's buffers are "
+                  "evicted by the others between its launches" % (total_bytes / 1e9, L2_BYTES >> 20),
+            "parallelism": "replicas of the per-GPU workload (weak scaling), no collective"}
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     if world > 1:
@@ -371,10 +380,7 @@ def run_ours(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtypes": "bf16,f16 (x: bf16; cos/sin f32)",
                 "data": "synthetic (seeded SplitMix64 + Box-Muller N(0,1); cos/sin tables from base 1e4 / 1e6)",
                 "tokens_per_s": round(tokens_per_s, 1),
-                "config": {"workload": WORKLOAD_NAME, "bytes_per_step": total_bytes, "tokens_per_step": step_tokens,
-                           "l2": "inputs larger than L2: %.2f GB per step vs %d MB L2; each kernel's buffers are "
-                                 "evicted by the others between its launches" % (total_bytes / 1e9, L2_BYTES >> 20),
-                           "parallelism": "replicas of the per-GPU workload (weak scaling), no collective"},
+                "config": step_config(total_bytes, step_tokens),
                 "per_kernel": kernels, "next_rows": next_rows, "small_rows": small, "roofline": roofline, "e2e": e2e,
                 "gpu_launches": launches,
                 "clocks": clocks, "cpu_baseline": cpu}
@@ -912,7 +918,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "tokens_per_s": round(tok / secs, 1),
-            "config": {"workload": WORKLOAD_NAME, "sample": sample},
+            "config": step_config(sum(algorithmic_bytes(c) for c in cases), sum(c.tokens for c in cases)),
+            "sample": sample,
             "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "nproc": host["nproc"], "cpu_model": host["cpu_model"], "sample": sample},
             "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -137,3 +137,22 @@ def test_the_unhashed_argument_checks_hold_no_kernel_or_launch():
     csrc = os.path.dirname(path)
     hashed = [n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")) and n != bench.ARGUMENT_CHECKS]
     assert {"rope_cache.cu", "rope_qkv.cu", "rope_launch.cu", "rope_inplace.cuh", "rope_device.cuh"} <= set(hashed)
+
+
+def test_reference_arm_reports_the_same_config_as_ours():
+    """The reference arm (the oracle on the host cores) prints the config that
+    our arm prints: the same workload, bytes and tokens per step."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(bench.__file__)
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3", "--reference-seconds", "0.5"], capture_output=True, text=True, check=True,
+                         cwd=root, timeout=600).stdout
+    line = json.loads(out.strip().splitlines()[-1])
+    cases = bench.build_workloads()
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.step_config(sum(bench.algorithmic_bytes(c) for c in cases),
+                                               sum(c.tokens for c in cases))
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
