@@ -329,6 +329,7 @@ def run_ours(args):
     specs = operator_specs(cases, dev_tensors)
     next_rows = time_next_rows(specs, calls, Kk)
     streams = time_streams(specs)
+    copy_us = {b: copy_stream_us(b) for b in set(step_bytes)}
     del specs
     for entry in next_rows:
         entry.update(streams.get(entry["workload"], {}))
@@ -348,7 +349,9 @@ def run_ours(args):
                         "avg_us": round(avg * 1e3, 3),
                         "median_us": round(statistics.median(ms) * 1e3, 3),
                         "gbs": round(b / (avg * 1e-3) / 1e9, 1), "frac_of_peak": round(b / (avg * 1e-3) / 1e9 / peak, 4),
-                        "tokens": c.tokens, **streams.get(kernel_label(c), {})})
+                        "tokens": c.tokens, **streams.get(kernel_label(c), {}),
+                        "copy_stream_us": round(copy_us[b], 3),
+                        "vs_copy": round(copy_us[b] / streams[kernel_label(c)]["stream_us"], 4)})
     dom = max(range(nk), key=lambda i: sum(per_kernel_ms[i]))
     dom_label = kernel_label(cases[dom])
     dom_avg_s = sum(per_kernel_ms[dom]) / Kk * 1e-3
@@ -591,6 +594,16 @@ def time_streams(specs, launches=200):
         out[label] = {"stream_us": round(us, 3), "stream_frac_of_peak": round(nbytes / (us * 1e-6) / 1e9 / peak, 4),
                       "stream_buffer_sets": n}
     return out
+
+
+def copy_stream_us(nbytes: int, launches: int = 200) -> float:
+    """Microseconds per launch of the device copy that defines the peak
+    (``copy_`` of bf16 buffers, nbytes / 2 read and nbytes / 2 written), timed
+    as stream_us times an operator: back to back over rotating buffer copies."""
+    n = max(1, nbytes // 4)  # bf16 elements per buffer
+    return stream_us(lambda k: [lambda s=torch.empty(n, dtype=torch.bfloat16, device="cuda"),
+                                       d=torch.empty(n, dtype=torch.bfloat16, device="cuda"): d.copy_(s)
+                                for _ in range(k)], 4 * n, launches)[0]
 
 
 def stream_us(factory, nbytes, launches=200):
