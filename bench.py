@@ -329,10 +329,13 @@ def run_ours(args):
     specs = operator_specs(cases, dev_tensors)
     next_rows = time_next_rows(specs, calls, Kk)
     streams = time_streams(specs)
-    copy_us = {b: copy_stream_us(b) for b in set(step_bytes)}
+    copy_us = {b: copy_stream_us(b) for b in set(step_bytes) | {nb for _, nb, _, _ in specs}}
     del specs
     for entry in next_rows:
         entry.update(streams.get(entry["workload"], {}))
+        if "stream_us" in entry:
+            entry["copy_stream_us"] = round(copy_us[entry["bytes_per_launch"]], 3)
+            entry["vs_copy"] = round(copy_us[entry["bytes_per_launch"]] / entry["stream_us"], 4)
     small = time_small_rows(dev)
     sampler.stop()
     clocks = sampler.summary(t_host0, t_host1)
