@@ -248,11 +248,11 @@ def step_config(total_bytes: int, step_tokens: int) -> dict:
 
 def run_ours(args):
     world, rank, local = dist_env()
+    torch.cuda.set_device(local)  # before the process group, so its collectives use this GPU
+    dev = torch.device("cuda", local)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
 
     from transformer_rope_positional_gb300 import build as B
     B.build()

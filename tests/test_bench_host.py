@@ -156,3 +156,35 @@ def test_reference_arm_reports_the_same_config_as_ours():
     assert line["config"] == bench.step_config(sum(bench.algorithmic_bytes(c) for c in cases),
                                                sum(c.tokens for c in cases))
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_library_builds_of_concurrent_processes_take_turns(tmp_path, monkeypatch):
+    """Ranks of a multi-GPU run build at once; the shared object files must not
+    be compiled by two of them together (the build holds a lock file)."""
+    import threading
+    import time
+
+    from transformer_rope_positional_gb300 import build as B
+
+    monkeypatch.setattr(B, "LIB_DIR", str(tmp_path))
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "librope_gb300.so"))
+    inside, most, calls = [0], [0], []
+    guard = threading.Lock()
+
+    def fake_build(lib_path, verbose, debug):
+        with guard:
+            inside[0] += 1
+            most[0] = max(most[0], inside[0])
+        time.sleep(0.2)
+        with guard:
+            inside[0] -= 1
+            calls.append(lib_path)
+        return lib_path
+
+    monkeypatch.setattr(B, "_build_locked", fake_build)
+    threads = [threading.Thread(target=B.build, kwargs={"force": True}) for _ in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert len(calls) == 4 and most[0] == 1

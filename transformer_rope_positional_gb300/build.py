@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -57,10 +58,24 @@ def up_to_date(lib: str = LIB_PATH) -> bool:
 
 def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
     """Compile every translation unit and link the shared library (the
-    bounds-checking debug library with ``debug=True``)."""
+    bounds-checking debug library with ``debug=True``).  Processes that build
+    at once (one per rank of a multi-GPU run) take turns on a lock file: the
+    object files share one build directory."""
     lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
     if not force and up_to_date(lib_path):
         return lib_path
+    os.makedirs(LIB_DIR, exist_ok=True)
+    with open(lib_path + ".lock", "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and up_to_date(lib_path):  # built while this process waited
+                return lib_path
+            return _build_locked(lib_path, verbose, debug)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(lib_path: str, verbose: bool, debug: bool) -> str:
     build_dir = BUILD_DIR + ("_debug" if debug else "")
     os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
