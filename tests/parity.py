@@ -8,8 +8,10 @@ Tolerances (written here, applied everywhere):
   the oracle rounds the binary64 result once, so the expected gap is below
   2.4e-7; 2e-6 is the stated bar.
 * float16 / bfloat16 outputs: at most ``HALF_ULP_TOL`` = 1 unit in the last place
-  of the output type.  The binary32 result is within 2^-23 of the exact value,
-  so narrowing it differs from narrowing the exact value by at most one ulp.
+  of the output type.  The binary32 result is within 2^-23 of the exact value
+  (Kahan's form; the 16-bit cache kernels that use one FMA after a product that
+  is exact in binary32 are correctly rounded), so narrowing it differs from
+  narrowing the exact value by at most one ulp.
 * columns the operator must not touch: bit-exact.
 * NaN matches NaN (any payload); +0 matches -0; infinities must match exactly.
 """
