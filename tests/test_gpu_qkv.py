@@ -183,3 +183,14 @@ def test_many_sequences(rope_gpu, num_seqs):
     case = W.qkv_case("many", 136, query_lens, context_lens, 4, 2, 1, 64, 16, torch.float16, pad_every=11)
     bp, bs = _check(case, _run_gpu(case), _run_oracle(case))
     assert bp == 0 and bs == 0 and R.get_device_error() == 0
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("block_size", [3, 5, 12, 24])
+def test_block_sizes_that_are_not_powers_of_two(rope_gpu, dt, block_size):
+    """A slot splits into (block, offset) by a shift when the block size is a
+    power of two and by a division otherwise: the division path."""
+    case = W.qkv_case("bs%d" % block_size, 137, [29, 1, 6, 1], [3, 77, 40, 0], 4, 2, 2, 128, block_size, dt,
+                      pad_every=5)
+    bp, bs = _check(case, _run_gpu(case), _run_oracle(case))
+    assert bp == 0 and bs == 0 and R.get_device_error() == 0
