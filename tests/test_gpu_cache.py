@@ -186,3 +186,18 @@ def test_rejected_arguments_raise(rope_gpu):
         R.rope_with_sin_cos_cache(case.positions.cuda(), case.query.cuda(), case.key.cuda(), case.cache.cuda(),
                                   48)
     assert e.value.status == R.ROPE_ERR_PARAM_INVALID
+
+
+@pytest.mark.parametrize("neox,section", [(True, None), (False, None), (True, [16, 24, 24])])
+def test_repeated_calls_are_bit_identical(rope_gpu, neox, section):
+    """Results do not depend on the run: the same call on fresh copies of the
+    inputs gives the same bits (no atomics or order-dependent sums on the path)."""
+    case = W.cache_case("det", 140, 3000, 8, 2, 128, 128, 5000, torch.bfloat16, neox, mrope_section=section)
+    pos, cache = case.positions.cuda(), case.cache.cuda()
+    outs = []
+    for _ in range(2):
+        q, k = case.query.cuda(), case.key.cuda()
+        R.rope_with_sin_cos_cache(pos, q, k, cache, 128, 128, neox, section)
+        torch.cuda.synchronize()
+        outs.append((q.cpu(), k.cpu()))
+    assert same_bits(outs[0][0], outs[1][0]) and same_bits(outs[0][1], outs[1][1])
