@@ -91,3 +91,39 @@ def test_cache_matches_complex_form_anywhere(problem):
         assert _ulp_dist(got, ref).max() <= 1
         heads_got, heads_x = got.reshape(T, -1, hs), x.reshape(T, -1, hs)
         assert _same_bits(heads_got[..., R:], heads_x[..., R:])
+
+
+@st.composite
+def qkv_problems(draw):
+    dt = draw(st.sampled_from(DTYPES))
+    D = draw(st.sampled_from([16, 32, 64, 96, 128]))
+    nq, nk, nv = draw(st.integers(0, 5)), draw(st.integers(0, 3)), draw(st.integers(0, 3))
+    if nq + nk + nv == 0:
+        nq = 1
+    B = draw(st.integers(1, 6))
+    qlens = draw(st.lists(st.integers(0, 9), min_size=B, max_size=B))
+    if sum(qlens) == 0:
+        qlens[0] = 1
+    ctx = draw(st.lists(st.integers(0, 60), min_size=B, max_size=B))
+    block = draw(st.sampled_from([1, 3, 4, 16]))
+    pad = draw(st.sampled_from([0, 0, 2, 5]))
+    return dt, D, nq, nk, nv, qlens, ctx, block, pad, draw(st.integers(0, 10_000))
+
+
+@settings(**SETTINGS)
+@given(qkv_problems())
+def test_fused_qkv_matches_independent_composition_anywhere(problem):
+    from test_oracle_pins import _qkv_reference
+    dt, D, nq, nk, nv, qlens, ctx, block, pad, seed = problem
+    case = W.qkv_case("prop", seed, qlens, ctx, nq, nk, nv, D, block, dt, pad_every=pad)
+    qo, kc, vc, bad_pos, bad_slot = oracle.qkv_rmsnorm_rope_cache(
+        case.qkv, case.nq, case.nk, case.nv, case.q_gamma, case.k_gamma, case.eps, case.cache, case.seq_lens,
+        case.query_start_loc, case.slot_mapping, case.q_out, case.k_cache, case.v_cache)
+    assert bad_pos == 0 and bad_slot == 0
+    rq, rk, rv = _qkv_reference(case)
+    # one rounding on each side of a float64 computation: within one ulp (a
+    # branch with no heads gives an empty tensor, nothing to compare)
+    for got, ref in ((qo, rq), (kc, rk)):
+        if got.numel():
+            assert _ulp_dist(got, oracle.round_to(ref, dt)).max() <= 1
+    assert _same_bits(vc, oracle.round_to(rv, dt))
