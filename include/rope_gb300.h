@@ -1,7 +1,7 @@
 /*
  * rope_gb300.h -- C ABI of the GB300 (sm_103a) rotary position embedding library.
  *
- * Two operators, each an asynchronous call on a caller-given CUDA stream:
+ * Three operators, each an asynchronous call on a caller-given CUDA stream:
  *
  *   rope_inplace_partial          in-place partial-slice RoPE on a BSND tensor
  *                                 (interleave or half mode), and its backward
@@ -15,6 +15,7 @@
  *         部分旋转位置编码接口详解与实现剖析"
  *  [RSCC] "CANN ops-transformer 旋转位置编码算子 RopeWithSinCosCache 深度解析：
  *         cache 化 RoPE 的计算原理与 aclnn 两段式调用实战"
+ *  [QKV]  the "aclnnQkvRmsNormRopeCacheWithKScale" documentation page
  *
  * Memory and ownership.  Every tensor is described by a rope_tensor_t that the
  * caller owns; `data` is a DEVICE pointer to contiguous row-major storage,
@@ -24,7 +25,10 @@
  * library allocates nothing, needs no workspace, and never synchronises the
  * stream (except rope_get_device_error, which says so).  The two-phase
  * "GetWorkspaceSize, then execute" interface of the pages collapses to one call
- * because the workspace is always zero bytes.
+ * because the workspace is always zero bytes.  (The fused op's kernel uses up to
+ * 64 KB of on-chip shared memory per CTA; the first call that needs more than
+ * 48 KB on a device raises the kernel's shared-memory limit there, once, with
+ * cudaFuncSetAttribute.)
  *
  * Arithmetic.  Half-precision inputs are widened to binary32; each output is
  * a two-term dot product evaluated with Kahan's FMA-based difference of
