@@ -67,3 +67,23 @@ def test_fused_op_output_overlapping_its_input(rope_gpu):
     R.qkv_rmsnorm_rope_cache(t[0], qc.nq, qc.nk, qc.nv, t[1], t[2], qc.eps, *t[3:])
     torch.cuda.synchronize()
     assert R.get_device_error() == 0
+
+
+@pytest.mark.parametrize("neox", [True, False])
+def test_key_columns_before_query_columns_are_accepted(rope_gpu, neox):
+    """q and k as disjoint column ranges of one buffer, k first (a negative
+    offset for the overlap check): accepted, and rotated as the oracle says."""
+    import oracle
+    from parity import assert_matches
+
+    case = W.cache_case("k_first", 135, 24, 2, 1, 64, 64, 100, torch.bfloat16, neox)
+    buf = torch.zeros(24, 4 * 64, dtype=torch.bfloat16, device="cuda")
+    k, q = buf[:, :64], buf[:, 128:256]  # columns [64, 128) stay untouched
+    k.copy_(case.key.cuda())
+    q.copy_(case.query.cuda())
+    R.rope_with_sin_cos_cache(case.positions.cuda(), q, k, case.cache.cuda(), 64, 64, neox)
+    torch.cuda.synchronize()
+    qr, kr, _ = oracle.rope_with_sin_cos_cache(case.positions, case.query, case.key, case.cache, 64, neox)
+    assert_matches(q.cpu(), qr, "query")
+    assert_matches(k.cpu(), kr, "key")
+    assert not buf[:, 64:128].any()
